@@ -1,0 +1,265 @@
+// C-ABI entry points: argument validation, kernel choice and launches.
+// Every function validates on the host before enqueueing anything, launches
+// on the caller's stream and never synchronises.
+
+#include <cstdio>
+#include <cstdarg>
+#include <string>
+
+#include "bitlinear.h"
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+bl_status fail(bl_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+bl_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return BL_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr int64_t kMaxK = 65536;
+
+bl_status check_dims(int64_t M, int64_t N, int64_t K, bool need_m) {
+  if ((need_m && M <= 0) || N <= 0 || K <= 0)
+    return fail(BL_ERR_INVALID_ARG, "dimensions must be positive (M=%lld N=%lld K=%lld)",
+                (long long)M, (long long)N, (long long)K);
+  if (K % 4) return fail(BL_ERR_INVALID_ARG, "K=%lld is not a multiple of 4", (long long)K);
+  if (K > kMaxK) return fail(BL_ERR_UNSUPPORTED, "K=%lld exceeds %lld", (long long)K, (long long)kMaxK);
+  if (N * K >= (int64_t(1) << 32))
+    return fail(BL_ERR_UNSUPPORTED, "N*K=%lld must be below 2^32", (long long)(N * K));
+  if (need_m && M > (int64_t(1) << 31) - 1) return fail(BL_ERR_UNSUPPORTED, "M=%lld too large", (long long)M);
+  return BL_OK;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+// ---- GEMV / small-M contraction launcher (any M; tokens in groups of mt per CTA)
+bl_status launch_gemv(const uint8_t* wp, const int8_t* xq, const float* scale, const float* gamma, void* out,
+                      int64_t M, int64_t N, int64_t K, bl::GemvOut mode, cudaStream_t s) {
+  const bool vec = (K % 64 == 0) && aligned(wp, 16) && aligned(xq, 16);
+  const int64_t Kp = (K + 63) / 64 * 64;
+  int mt = M == 1 ? 1 : (M == 2 ? 2 : 4);
+  while (mt > 1 && mt * Kp > 200 * 1024) mt >>= 1;
+  const int warps_per_cta = bl::kGemvThreads / 32;
+  const int64_t want = (N + warps_per_cta - 1) / warps_per_cta;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
+  const int gx = static_cast<int>(want < cap ? want : cap);
+  if ((M + mt - 1) / mt > 65535) return fail(BL_ERR_UNSUPPORTED, "M=%lld too large for the GEMV grid", (long long)M);
+  cudaError_t e = bl::launch_gemv(wp, xq, scale, gamma, out, static_cast<int>(M), static_cast<int>(N),
+                                  static_cast<int>(K), mode, vec, mt, gx, s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemv_w2a8: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
+bl_status launch_act_quant(const void* x, bl_dtype dt, int64_t M, int64_t K, int8_t* xq, float* scale,
+                           cudaStream_t s) {
+  cudaError_t e = bl::launch_act_quant(x, dt == BL_BF16, static_cast<int>(M), static_cast<int>(K), xq, scale, s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_act_quant: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bitlinear_strerror(bl_status st) {
+  switch (st) {
+    case BL_OK: return "ok";
+    case BL_ERR_INVALID_ARG: return "invalid argument";
+    case BL_ERR_UNSUPPORTED: return "unsupported arguments";
+    case BL_ERR_CUDA: return "CUDA error";
+    case BL_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+const char* bitlinear_last_error(void) { return g_last_error.c_str(); }
+
+int bitlinear_version(void) { return 1; }
+
+size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K) {
+  (void)N;
+  (void)K;
+  return static_cast<size_t>(bl::kMaxAbsumCtas) * bl::kPartialWords * sizeof(uint32_t);
+}
+
+namespace {
+
+bl_status check_pack_args(const float* W, int64_t N, int64_t K, const void* Wp_or_null, const void* gamma) {
+  if (bl_status st = check_dims(1, N, K, false)) return st;
+  if (!W || !gamma) return fail(BL_ERR_INVALID_ARG, "null pointer (W or gamma)");
+  if (!aligned(W, 16)) return fail(BL_ERR_INVALID_ARG, "W must be 16-byte aligned");
+  if (Wp_or_null && !aligned(Wp_or_null, 16)) return fail(BL_ERR_INVALID_ARG, "Wp must be 16-byte aligned");
+  if (!aligned(gamma, 4)) return fail(BL_ERR_INVALID_ARG, "gamma must be 4-byte aligned");
+  return BL_OK;
+}
+
+bl_status run_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* workspace, cudaStream_t s) {
+  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
+  const uint64_t n4 = nk / 4;
+  const int sms = sm_count();
+  uint64_t ga = (n4 + bl::kAbsumThreads * 4 - 1) / (bl::kAbsumThreads * 4);
+  const uint64_t cap = static_cast<uint64_t>(sms) * 4 < static_cast<uint64_t>(bl::kMaxAbsumCtas)
+                           ? static_cast<uint64_t>(sms) * 4
+                           : static_cast<uint64_t>(bl::kMaxAbsumCtas);
+  if (ga > cap) ga = cap;
+  if (ga < 1) ga = 1;
+  uint32_t* partials = static_cast<uint32_t*>(workspace);
+  bl::bl_absum_partials<<<static_cast<unsigned>(ga), bl::kAbsumThreads, 0, s>>>(
+      reinterpret_cast<const float4*>(W), n4, partials);
+  if (bl_status st = check_launch("bl_absum_partials")) return st;
+  bl::bl_gamma_finalize<<<1, 256, 0, s>>>(partials, static_cast<int>(ga), nk, gamma);
+  return check_launch("bl_gamma_finalize");
+}
+
+bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma, uint8_t* Wp, cudaStream_t s) {
+  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
+  const uint64_t n_bytes = nk / 4;
+  const uint64_t n_words = n_bytes / 4;
+  const int sms = sm_count();
+  uint64_t gq = (n_words + 255) / 256;
+  if (gq > static_cast<uint64_t>(sms) * 8) gq = static_cast<uint64_t>(sms) * 8;
+  if (gq < 1) gq = 1;
+  bl::bl_quant_pack<<<static_cast<unsigned>(gq), 256, 0, s>>>(reinterpret_cast<const float4*>(W), n_bytes, gamma,
+                                                               reinterpret_cast<uint32_t*>(Wp));
+  return check_launch("bl_quant_pack");
+}
+
+bl_status check_pack_workspace(int64_t N, int64_t K, const void* workspace, size_t ws_bytes) {
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < bitlinear_pack_workspace_bytes(N, K))
+    return fail(BL_ERR_WORKSPACE, "pack workspace needs %zu bytes, 256-byte aligned",
+                bitlinear_pack_workspace_bytes(N, K));
+  return BL_OK;
+}
+
+}  // namespace
+
+bl_status bitlinear_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* workspace, size_t ws_bytes,
+                            bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_pack_args(W, N, K, nullptr, gamma)) return st;
+  if (bl_status st = check_pack_workspace(N, K, workspace, ws_bytes)) return st;
+  return run_absmean(W, N, K, gamma, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bl_status bitlinear_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma, uint8_t* Wp,
+                                  bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_pack_args(W, N, K, Wp, gamma)) return st;
+  if (!Wp) return fail(BL_ERR_INVALID_ARG, "null pointer (Wp)");
+  return run_quantize_pack(W, N, K, gamma, Wp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, uint8_t* Wp, float* gamma,
+                                 void* workspace, size_t ws_bytes, bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_pack_args(W, N, K, Wp, gamma)) return st;
+  if (!Wp) return fail(BL_ERR_INVALID_ARG, "null pointer (Wp)");
+  if (bl_status st = check_pack_workspace(N, K, workspace, ws_bytes)) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (bl_status st = run_absmean(W, N, K, gamma, workspace, s)) return st;
+  return run_quantize_pack(W, N, K, gamma, Wp, s);
+}
+
+bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K, int8_t* xq, float* scale,
+                              bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_dims(M, 1, K, true)) return st;
+  if (dt != BL_F32 && dt != BL_BF16) return fail(BL_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!x || !xq || !scale) return fail(BL_ERR_INVALID_ARG, "null pointer (x, xq or scale)");
+  if (!aligned(x, 16) || !aligned(xq, 16) || !aligned(scale, 4))
+    return fail(BL_ERR_INVALID_ARG, "x and xq must be 16-byte aligned, scale 4-byte aligned");
+  return launch_act_quant(x, dt, M, K, xq, scale, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  if (M <= 0 || K <= 0) return 0;
+  return align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) + align_up(static_cast<size_t>(M) * 4, 256);
+}
+
+bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t* Wp, const float* gamma,
+                            int64_t N, int64_t K, float* y, int8_t* xq_out, float* scale_out, void* workspace,
+                            size_t ws_bytes, bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_dims(M, N, K, true)) return st;
+  if (dt != BL_F32 && dt != BL_BF16) return fail(BL_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!x || !Wp || !gamma || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (x, Wp, gamma or y)");
+  if (!aligned(x, 16) || !aligned(Wp, 16) || !aligned(y, 16) || !aligned(gamma, 4))
+    return fail(BL_ERR_INVALID_ARG, "x, Wp and y must be 16-byte aligned, gamma 4-byte aligned");
+  if (xq_out && !aligned(xq_out, 16)) return fail(BL_ERR_INVALID_ARG, "xq_out must be 16-byte aligned");
+  if (scale_out && !aligned(scale_out, 4)) return fail(BL_ERR_INVALID_ARG, "scale_out must be 4-byte aligned");
+  const size_t need = bitlinear_forward_workspace_bytes(M, N, K);
+  if (need && (!workspace || !aligned(workspace, 256) || ws_bytes < need))
+    return fail(BL_ERR_WORKSPACE, "forward workspace needs %zu bytes, 256-byte aligned", need);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int8_t* xq = xq_out ? xq_out : reinterpret_cast<int8_t*>(ws);
+  float* sc = scale_out ? scale_out
+                        : reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256));
+  if (bl_status st = launch_act_quant(x, dt, M, K, xq, sc, s)) return st;
+  return launch_gemv(Wp, xq, sc, gamma, y, M, N, K, bl::GemvOut::kY, s);
+}
+
+size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;
+}
+
+bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const uint8_t* Wp, const float* gamma,
+                         int64_t N, int64_t K, float* y, void* workspace, size_t ws_bytes, bl_stream_t stream) {
+  g_last_error.clear();
+  (void)workspace;
+  (void)ws_bytes;
+  if (bl_status st = check_dims(M, N, K, true)) return st;
+  if (!xq || !scale || !Wp || !gamma || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (xq, scale, Wp, gamma or y)");
+  if (!aligned(xq, 16) || !aligned(Wp, 16) || !aligned(y, 16) || !aligned(scale, 4) || !aligned(gamma, 4))
+    return fail(BL_ERR_INVALID_ARG, "xq, Wp and y must be 16-byte aligned, scale and gamma 4-byte aligned");
+  return launch_gemv(Wp, xq, scale, gamma, y, M, N, K, bl::GemvOut::kY, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t bitlinear_gemm_i32_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;
+}
+
+bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp, int64_t M, int64_t N, int64_t K, int32_t* acc,
+                             void* workspace, size_t ws_bytes, bl_stream_t stream) {
+  g_last_error.clear();
+  (void)workspace;
+  (void)ws_bytes;
+  if (bl_status st = check_dims(M, N, K, true)) return st;
+  if (!xq || !Wp || !acc) return fail(BL_ERR_INVALID_ARG, "null pointer (xq, Wp or acc)");
+  if (!aligned(xq, 16) || !aligned(Wp, 16) || !aligned(acc, 16))
+    return fail(BL_ERR_INVALID_ARG, "xq, Wp and acc must be 16-byte aligned");
+  return launch_gemv(Wp, xq, nullptr, nullptr, acc, M, N, K, bl::GemvOut::kAcc,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Shared device helpers for the BitLinear W1.58A8 kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "bitlinear.h"
+
+#define BL_DEVICE __device__ __forceinline__
+
+namespace bl {
+
+constexpr float kEpsGamma = 1e-5f;    // added to gamma in the quantisation divisor
+constexpr float kEpsAbsmax = 1e-5f;   // floor on the per-token absmax
+
+// Packed field of a ternary code: field = code + 1.
+//   code = 0  <=>  |w| <= d/2   (w/d rounds to a value <= 0.5, and rint(0.5) = 0)
+//   code = +-1 otherwise, with the sign of w.
+// For a normal fp32 divisor d the two predicates agree bit for bit with
+// clip(rint(RN(w/d)), -1, 1): the fp32 quotient of a value just above d/2 is
+// at least 0.5 + 2^-24, because w = d/2 + ulp(d/2) gives w/d = 0.5 + 1/(2M)
+// with M < 2^24 the significand of d, which lies above the midpoint
+// 0.5 + 2^-25 between 0.5 and its successor.
+BL_DEVICE uint32_t ternary_field(float w, float half_d) {
+  return fabsf(w) > half_d ? (w > 0.f ? 2u : 0u) : 1u;
+}
+
+BL_DEVICE int dp4a_us(uint32_t a_u8x4, int b_s8x4, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a_u8x4), "r"(b_s8x4), "r"(c));
+  return d;
+}
+
+BL_DEVICE int dp4a_ss(int a, int b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 4x4 byte transpose of a 16-byte block: out word i, byte j = in word j, byte i.
+BL_DEVICE void transpose4x4_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                  uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  // pairs first: (a,b) -> bytes {a0 b0 a1 b1}, {a2 b2 a3 b3}
+  uint32_t ab_lo = __byte_perm(a, b, 0x5140);
+  uint32_t ab_hi = __byte_perm(a, b, 0x7362);
+  uint32_t cd_lo = __byte_perm(c, d, 0x5140);
+  uint32_t cd_hi = __byte_perm(c, d, 0x7362);
+  o0 = __byte_perm(ab_lo, cd_lo, 0x5410);   // a0 b0 c0 d0
+  o1 = __byte_perm(ab_lo, cd_lo, 0x7632);   // a1 b1 c1 d1
+  o2 = __byte_perm(ab_hi, cd_hi, 0x5410);   // a2 b2 c2 d2
+  o3 = __byte_perm(ab_hi, cd_hi, 0x7632);   // a3 b3 c3 d3
+}
+
+BL_DEVICE float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+BL_DEVICE int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Per-token scale and code, as fp32 operations with round-to-nearest-even.
+BL_DEVICE float token_scale(float absmax) {
+  return __fdiv_rn(127.0f, fmaxf(absmax, kEpsAbsmax));
+}
+
+BL_DEVICE int quant_code(float x, float s) {
+  int q = __float2int_rn(__fmul_rn(x, s));
+  return min(127, max(-128, q));
+}
+
+BL_DEVICE float bf16_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+BL_DEVICE float rescale(int acc, float gamma, float s) {
+  return __fdiv_rn(__fmul_rn(static_cast<float>(acc), gamma), s);
+}
+
+}  // namespace bl

@@ -1,0 +1,37 @@
+// Kernel declarations shared by the C-ABI layer and the kernel sources.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bl {
+
+// ---- weight packing (pack.cu)
+constexpr int kAbsumThreads = 256;
+constexpr int kPartialWords = 16;          // one 64-byte exact partial per CTA (12 limbs used)
+constexpr int kMaxAbsumCtas = 1184;        // 8 per SM on 148 SMs
+
+__global__ void bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials);
+__global__ void bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_t count,
+                                  float* __restrict__ gamma);
+__global__ void bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __restrict__ gamma,
+                              uint32_t* __restrict__ wp_words);
+
+// ---- activation quantisation (act_quant.cu)
+constexpr int kActThreads = 256;
+// x is fp32 (bf16 == false) or bf16 bits (bf16 == true); one CTA per token.
+cudaError_t launch_act_quant(const void* x, bool bf16, int M, int K, int8_t* xq, float* scale, cudaStream_t s);
+
+// ---- decode GEMV (gemv.cu)
+constexpr int kGemvThreads = 512;          // 16 warps, one output row per warp at a time
+constexpr int kGemvMaxTokens = 4;          // tokens per CTA (grid.y covers larger M)
+
+enum class GemvOut { kY = 0, kAcc = 1 };
+
+// out is fp32 y [M][N] (kY) or int32 acc [M][N] (kAcc); scale/gamma unused for kAcc.
+// vec selects 16-byte weight loads (K % 64 == 0, 16-byte aligned rows); mt is
+// the number of tokens per CTA (1, 2 or 4); grid_x CTAs of kGemvThreads.
+cudaError_t launch_gemv(const uint8_t* wp, const int8_t* xq, const float* scale, const float* gamma, void* out,
+                        int M, int N, int K, GemvOut mode, bool vec, int mt, int grid_x, cudaStream_t s);
+
+}  // namespace bl

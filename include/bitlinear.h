@@ -1,0 +1,203 @@
+/*
+ * bitlinear.h -- C ABI of the B300 BitLinear W1.58A8 forward library.
+ *
+ * The operation (BitNet b1.58 BitLinear, weights 1.58-bit, activations 8-bit):
+ *
+ *   gamma   = mean(|W|)                                   per tensor, fp32
+ *   code    = clip(rint(W / (gamma + 1e-5)), -1, 1)       ternary weight codes
+ *   Wp      = four codes per byte                         packed weights
+ *   s_m     = 127 / max(max_k |x[m][k]|, 1e-5)            per-token scale, fp32
+ *   x_q     = clip(rint(x * s_m), -128, 127)              int8 activations
+ *   acc     = sum_k code[n][k] * x_q[m][k]                exact int32
+ *   y[m][n] = acc * gamma / s_m                           fp32 output
+ *
+ * Sources (web pages, cited by title and section):
+ *   "BitNet 1-bit LLM 的混合精度微调技术：渐进量化策略" (blog.hotdry.top), body,
+ *     the quantisation-function paragraph (weight absmean = mean(|W|),
+ *     activation absmax = max(|X|, eps = 1e-5)) and the forward-pass sentence
+ *     (divide by the absmean factor, round, limit to [-1, 1], multiply back;
+ *     activations absmax-quantised per token to 8 bits).
+ *   "穿越1比特的奇幻旅程：高效语言模型的未来之谜" (summary of the BitNet b1.58
+ *     2B4T Technical Report), section "架构创新：量化魔法的背后" (absmean
+ *     ternary weights, per-token absmax INT8 activations, no bias) and section
+ *     "GPU端：CUDA内核的定制魔法" (W1.58A8 matmul; four ternary weights packed
+ *     into one 8-bit value: pack, store, load, unpack, compute).
+ *   "BitNet 中使用直通估计器工程化三元权重训练" (blog.hotdry.top), section
+ *     "STE 机制在三元训练中的作用" (torch.round: ties to even).
+ *
+ * Numerical contract (every step is deterministic and bit-reproducible):
+ *   - gamma is the exact mean of |W| rounded once to fp32, ties to even;
+ *   - d = fp32(gamma + 1e-5f); code = clip(rint(fp32(W / d)), -1, 1);
+ *   - s_m = fp32(127 / fp32 max(absmax, 1e-5f)); x_q = clip(rint(fp32(x * s_m)));
+ *   - y = fp32(fp32((float)acc * gamma) / s_m);
+ *   - every rounding is round-to-nearest, ties to even.
+ *
+ * Packed layout: Wp is uint8 [N][K/4], row-major. Byte j of row n holds the
+ * codes of k = 4j .. 4j+3; the code of k = 4j+i sits in bits 2i..2i+1 as the
+ * field value code + 1 (0 -> -1, 1 -> 0, 2 -> +1; 3 never occurs).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers unless stated otherwise; the caller owns
+ *     and allocates every buffer. The library never allocates device memory
+ *     on the compute path.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: nothing synchronises the host.
+ *   - Argument errors are detected on the host before any launch and return
+ *     a non-zero status with nothing enqueued. Launch errors return
+ *     BL_ERR_CUDA. Errors while kernels run surface at the caller's next
+ *     synchronisation, as for any CUDA work.
+ *   - x, W, Wp, x_q and y must be 16-byte aligned. M, N, K > 0, K % 4 == 0,
+ *     N * K < 2^32 and K <= 65536 (the int32 accumulator of |acc| <= 127*K).
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ *   - The functions are thread-safe; the last error message is thread-local.
+ */
+#ifndef BITLINEAR_H
+#define BITLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BL_API __attribute__((visibility("default")))
+#else
+#define BL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BL_OK = 0,
+    BL_ERR_INVALID_ARG = 1,   /* a pointer, size, alignment or dtype is invalid */
+    BL_ERR_UNSUPPORTED = 2,   /* valid arguments this build does not handle */
+    BL_ERR_CUDA = 3,          /* a CUDA call failed; see bitlinear_last_error() */
+    BL_ERR_WORKSPACE = 4      /* workspace missing, misaligned or too small */
+} bl_status;
+
+typedef enum {
+    BL_F32 = 0,               /* activations are fp32 */
+    BL_BF16 = 1               /* activations are bf16 (widened exactly to fp32) */
+} bl_dtype;
+
+/* Same type as cudaStream_t, declared without including CUDA headers. */
+typedef struct CUstream_st* bl_stream_t;
+
+/* ---------------------------------------------------------------------------
+ * Weight quantisation and packing (absmean, ternary codes, 4 codes per byte).
+ * Passages: the quantisation-function paragraph and forward-pass sentence of
+ * "BitNet 1-bit LLM 的混合精度微调技术"; sections "架构创新" and "GPU端" of the
+ * 2B4T summary.
+ *
+ * W         fp32 [N][K] row-major (nn.Linear layout: out x in), read only.
+ * Wp        uint8 [N][K/4], written.
+ * gamma     one fp32, written (device pointer).
+ * workspace at least bitlinear_pack_workspace_bytes(N, K) bytes, 256-byte
+ *           aligned, used as scratch for the exact sum; no initial contents
+ *           are needed and none survive the call.
+ * ------------------------------------------------------------------------- */
+BL_API size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K);
+
+BL_API bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K,
+                                 uint8_t* Wp, float* gamma,
+                                 void* workspace, size_t ws_bytes,
+                                 bl_stream_t stream);
+
+/* The two halves of bitlinear_pack_weights, for callers that need gamma alone
+ * or time the steps separately.
+ *
+ * bitlinear_absmean: gamma = mean(|W|), exact sum rounded once to fp32.
+ *   workspace: at least bitlinear_pack_workspace_bytes(N, K) bytes, 256-byte
+ *   aligned, scratch only.
+ * bitlinear_quantize_pack: codes clip(rint(W / (gamma + 1e-5)), -1, 1) packed
+ *   four per byte into Wp, with gamma read from device memory (as written by
+ *   bitlinear_absmean, or any fp32 value >= 0). */
+BL_API bl_status bitlinear_absmean(const float* W, int64_t N, int64_t K, float* gamma,
+                                   void* workspace, size_t ws_bytes, bl_stream_t stream);
+
+BL_API bl_status bitlinear_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma,
+                                         uint8_t* Wp, bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Per-token absmax int8 activation quantisation.
+ * Passages: "activation absmax = max(|X|, eps=1e-5)" and per-token 8-bit
+ * quantisation in "BitNet 1-bit LLM 的混合精度微调技术"; INT8 per-token absmax in
+ * section "架构创新" of the 2B4T summary.
+ *
+ * x      [M][K] row-major, fp32 or bf16 per `dt`, read only.
+ * xq     int8 [M][K] row-major, written.
+ * scale  fp32 [M], written: s_m = 127 / max(max|x_m|, 1e-5).
+ * ------------------------------------------------------------------------- */
+BL_API bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K,
+                              int8_t* xq, float* scale, bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The forward: activation quantisation, ternary x int8 contraction with an
+ * exact int32 accumulator and the fp32 rescale y = acc * gamma / s.
+ * Passages: section "GPU端：CUDA内核的定制魔法" of the 2B4T summary (W1.58A8
+ * matmul over packed weights); "multiply back by the factor" in the
+ * forward-pass sentence of "BitNet 1-bit LLM 的混合精度微调技术".
+ *
+ * x          [M][K] row-major activations, fp32 or bf16 per `dt`.
+ * Wp, gamma  from bitlinear_pack_weights.
+ * y          fp32 [M][N] row-major, written.
+ * xq_out     optional int8 [M][K]: if non-NULL the quantised activations are
+ *            also written there.
+ * scale_out  optional fp32 [M]: if non-NULL the per-token scales are written.
+ * workspace  at least bitlinear_forward_workspace_bytes(M, N, K) bytes,
+ *            256-byte aligned (may be NULL when that size is 0).
+ *
+ * The kernel is chosen by M: a dp4a GEMV for M <= 4, tcgen05 tensor-core
+ * kernels otherwise.
+ * ------------------------------------------------------------------------- */
+BL_API size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+BL_API bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M,
+                            const uint8_t* Wp, const float* gamma,
+                            int64_t N, int64_t K, float* y,
+                            int8_t* xq_out, float* scale_out,
+                            void* workspace, size_t ws_bytes,
+                            bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The contraction and rescale on already-quantised activations:
+ * y[m][n] = fp32(fp32(acc[m][n] * gamma) / scale[m]).
+ * Passages: as for bitlinear_forward.
+ *
+ * xq         int8 [M][K] row-major, scale fp32 [M] (from bitlinear_quant_act).
+ * workspace  at least bitlinear_gemm_workspace_bytes(M, N, K) bytes, 256-byte
+ *            aligned (may be NULL when that size is 0).
+ * ------------------------------------------------------------------------- */
+BL_API size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+BL_API bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M,
+                                const uint8_t* Wp, const float* gamma, int64_t N, int64_t K,
+                                float* y, void* workspace, size_t ws_bytes, bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The bare contraction acc[m][n] = sum_k code[n][k] * xq[m][k] (exact int32),
+ * for checking the accumulator bit for bit.
+ * Passage: section "GPU端：CUDA内核的定制魔法" of the 2B4T summary.
+ *
+ * xq   int8 [M][K] row-major; Wp uint8 [N][K/4]; acc int32 [M][N], written.
+ * workspace at least bitlinear_gemm_i32_workspace_bytes(M, N, K) bytes.
+ * ------------------------------------------------------------------------- */
+BL_API size_t bitlinear_gemm_i32_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+BL_API bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp,
+                             int64_t M, int64_t N, int64_t K, int32_t* acc,
+                             void* workspace, size_t ws_bytes,
+                             bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics.
+ * ------------------------------------------------------------------------- */
+BL_API const char* bitlinear_strerror(bl_status status);   /* static string */
+BL_API const char* bitlinear_last_error(void);             /* thread-local detail of the last failure */
+BL_API int bitlinear_version(void);                        /* ABI version, currently 1 */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H */

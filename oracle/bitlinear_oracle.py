@@ -93,21 +93,29 @@ def round_ratio_to_f32(num: int, den: int) -> np.float32:
 def exact_abs_sum(w) -> Fraction:
     """Exact sum of |W| as a rational number.
 
-    Every finite fp32 value is m * 2^(e-24) with an integer m < 2^24, so the
-    sum over all elements is a finite sum of integers times powers of two;
-    per-exponent integer sums are exact in int64 and are combined as Python
-    rationals.
+    By the IEEE-754 binary32 definition, a value with biased exponent field
+    e and fraction field f is (2^23 + f) * 2^(e - 150) when e >= 1 and
+    f * 2^-149 when e = 0, so |W| summed over all elements is a finite sum of
+    integers times powers of two. The integer significands are summed per
+    exponent field; each is split into two 12-bit halves so that every
+    per-exponent sum stays below 2^53 (up to 2^41 elements) and is therefore
+    exact in the fp64 accumulator of bincount. The 256 per-exponent sums are
+    then combined as Python rationals.
     """
-    a = np.abs(np.asarray(w, dtype=np.float32)).ravel().astype(np.float64)
-    if not np.all(np.isfinite(a)):
+    b = np.ascontiguousarray(np.asarray(w, dtype=np.float32)).ravel().view(np.uint32)
+    e = ((b >> 23) & 0xFF).astype(np.int64)
+    if np.any(e == 0xFF):
         raise ValueError("exact_abs_sum: non-finite input")
-    mant, expo = np.frexp(a)                      # a = mant * 2^expo, mant in [0.5, 1)
-    mi = np.ldexp(mant, 24).astype(np.int64)      # exact: fp32 has 24 significant bits
+    if b.size >= 2 ** 41:
+        raise ValueError("exact_abs_sum: too many elements for exact per-exponent sums")
+    frac = b & 0x7FFFFF
+    sig = np.where(e > 0, frac | 0x800000, frac)             # integer significand
+    hi = np.bincount(e, weights=(sig >> 12).astype(np.float64), minlength=256)
+    lo = np.bincount(e, weights=(sig & 0xFFF).astype(np.float64), minlength=256)
     total = Fraction(0)
-    nz = mi != 0
-    for e in np.unique(expo[nz]):
-        s = int(mi[expo == e].sum(dtype=np.int64))
-        total += Fraction(s) * Fraction(2) ** (int(e) - 24)
+    for ex in np.nonzero((hi != 0) | (lo != 0))[0]:
+        s = int(hi[ex]) * 4096 + int(lo[ex])
+        total += Fraction(s) * Fraction(2) ** (max(int(ex), 1) - 150)
     return total
 
 

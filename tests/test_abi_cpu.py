@@ -1,0 +1,102 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+reports its constants, and rejects bad arguments on the host before any CUDA
+call is made."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bitlinear.h")
+
+
+@pytest.fixture(scope="module")
+def blt():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bl_build", os.path.join(ROOT, "bit_ternary_forward_b300", "build.py"))
+    build = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build)
+    build.build()
+    import bit_ternary_forward_b300 as b
+    return b
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(bitlinear_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("bitlinear_pack_weights", "bitlinear_quant_act", "bitlinear_forward", "bitlinear_gemm_i32"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(blt):
+    lib = ctypes.CDLL(blt.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_library_exports_nothing_else(blt):
+    # the C ABI is the only public surface (kernels and helpers are hidden)
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", blt.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {n for n in exported if n.startswith("bitlinear_")}
+    assert ours == set(declared_functions())
+
+
+def test_constants(blt):
+    lib = blt.lib
+    assert lib.bitlinear_version() == 1
+    assert lib.bitlinear_strerror(0) == b"ok"
+    assert b"invalid" in lib.bitlinear_strerror(1)
+    assert lib.bitlinear_pack_workspace_bytes(6912, 2560) >= 64 * 148
+    assert lib.bitlinear_forward_workspace_bytes(4, 256, 256) >= 4 * 256
+    assert lib.bitlinear_forward_workspace_bytes(0, 256, 256) == 0
+
+
+@pytest.mark.parametrize("n,k", [(0, 256), (8, 0), (8, 6), (8, 70000), (1 << 20, 1 << 12)])
+def test_pack_rejects_bad_dims_on_host(blt, n, k):
+    lib = blt.lib
+    st = lib.bitlinear_pack_weights(16, n, k, 16, 16, 256, 1 << 20, None)
+    assert st in (blt.BL_ERR_INVALID_ARG, blt.BL_ERR_UNSUPPORTED)
+    assert lib.bitlinear_last_error()
+
+
+def test_pack_rejects_null_misaligned_and_workspace(blt):
+    lib = blt.lib
+    ws = lib.bitlinear_pack_workspace_bytes(64, 64)
+    assert lib.bitlinear_pack_weights(None, 64, 64, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_pack_weights(8, 64, 64, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG      # W misaligned
+    assert lib.bitlinear_pack_weights(16, 64, 64, 16, 16, None, ws, None) == blt.BL_ERR_WORKSPACE
+    assert lib.bitlinear_pack_weights(16, 64, 64, 16, 16, 128, ws, None) == blt.BL_ERR_WORKSPACE       # not 256-aligned
+    assert lib.bitlinear_pack_weights(16, 64, 64, 16, 16, 256, ws - 1, None) == blt.BL_ERR_WORKSPACE
+
+
+def test_forward_and_quant_reject_bad_args_on_host(blt):
+    lib = blt.lib
+    ws = lib.bitlinear_forward_workspace_bytes(4, 64, 64)
+    assert lib.bitlinear_forward(16, 7, 4, 16, 16, 64, 64, 16, None, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_forward(16, 1, 0, 16, 16, 64, 64, 16, None, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 62, 16, None, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 64, 24, None, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 64, 16, 8, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 64, 16, None, None, None, ws, None) == blt.BL_ERR_WORKSPACE
+    assert lib.bitlinear_quant_act(16, 1, 4, 6, 16, 16, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_quant_act(None, 1, 4, 8, 16, 16, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_gemm_i32(16, 16, 4, 4, 6, 16, None, 0, None) == blt.BL_ERR_INVALID_ARG
+    assert lib.bitlinear_gemm_i32(16, 16, 4, 4, 8, 20, None, 0, None) == blt.BL_ERR_INVALID_ARG
+
+
+def test_python_binding_rejects_cpu_tensors(blt):
+    import torch
+    with pytest.raises(TypeError):
+        blt.pack_weights(torch.zeros(4, 4))
+    with pytest.raises(TypeError):
+        blt.quant_act(torch.zeros(4, 4))

@@ -1,0 +1,163 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Bit-exact on gamma, packed bytes, x_q, per-token scales and the int32
+accumulators; y is checked both within 1e-6 relative (the stated tolerance)
+and bit for bit (the kernels evaluate the rescale in the oracle's order).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_common import bits, compare_full, compare_sampled_rows, gpu_run, oracle_weights, x_to_oracle
+from workloads import WORKLOADS, gaussian_activations, gaussian_weights, make_projection_inputs
+from workloads.synth import student_t_weights
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect -m gpu
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+import bit_ternary_forward_b300 as blt  # noqa: E402  (fails loudly if the library is missing)
+
+
+# ------------------------------------------------------------------ the five workloads
+def test_cpu_small_every_output():
+    p = WORKLOADS["cpu_small"].projections[0]
+    w, x = make_projection_inputs(p)
+    compare_full(w, x)
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_decode_2b_every_output(idx):
+    p = WORKLOADS["decode_2b"].projections[idx]
+    w, x = make_projection_inputs(p)
+    compare_full(w, x)
+
+
+@pytest.mark.parametrize("idx", range(6))
+def test_skinny_2b_outliers_every_output(idx):
+    p = WORKLOADS["skinny_2b"].projections[idx]
+    w, x = make_projection_inputs(p)
+    compare_full(w, x)
+
+
+@pytest.mark.parametrize("idx", [0, 1])
+def test_prefill_2b_sampled_tokens(idx):
+    p = WORKLOADS["prefill_2b"].projections[idx]
+    w, x = make_projection_inputs(p)
+    rows = np.sort(np.random.default_rng(idx).choice(p.m, 48, replace=False))
+    rows = np.concatenate([[0, p.m - 1], rows])
+    compare_sampled_rows(w, x, rows)
+
+
+@pytest.mark.parametrize("proj", range(4))
+def test_stack_7b_layer0_decode_every_output(proj):
+    p = WORKLOADS["stack_7b_decode"].projections[proj]
+    w, x = make_projection_inputs(p)
+    compare_full(w, x)
+
+
+@pytest.mark.parametrize("proj", [1, 3])
+def test_stack_7b_last_layer_prefill_sampled(proj):
+    p = WORKLOADS["stack_7b_prefill"].projections[31 * 4 + proj]
+    w, x = make_projection_inputs(p)
+    rows = np.array([0, 1, 777, 1500, 2047])
+    compare_sampled_rows(w, x, rows)
+
+
+# ------------------------------------------------------------------ shapes and tails
+@pytest.mark.parametrize("m,n,k", [
+    (1, 1, 4), (1, 3, 8), (2, 5, 12), (3, 7, 100), (5, 9, 64), (4, 33, 192), (2, 17, 1028),
+    (7, 65, 320), (9, 31, 4096), (1, 130, 65536), (4, 64, 65536), (17, 129, 960), (64, 300, 2560),
+    (65, 257, 128), (129, 96, 1088),
+])
+@pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float32])
+def test_shapes(m, n, k, xdt):
+    w = gaussian_weights(n, k, seed=1000 + n + k)
+    x = gaussian_activations(m, k, seed=2000 + m + k, dtype=xdt)
+    compare_full(w, x)
+
+
+# ------------------------------------------------------------------ degenerate and special values
+def test_zero_token_and_zero_weights():
+    w = gaussian_weights(64, 256, seed=5)
+    x = gaussian_activations(6, 256, seed=6)
+    x[2] = 0
+    x[4, :] = 0
+    compare_full(w, x)
+    compare_full(torch.zeros(32, 128), gaussian_activations(3, 128, seed=7))
+
+
+def test_gamma_tie_element():
+    from pins import _tie_tensor
+    wt, g, t = _tie_tensor()                    # contains +-t with t == (gamma + 1e-5)/2 exactly
+    w = torch.from_numpy(wt.copy())
+    r = gpu_run(w, gaussian_activations(2, w.shape[1], seed=8))
+    assert bits(r["gamma"]) == bits(g)
+    codes = oracle.unpack_codes(r["packed"]).ravel()
+    assert codes[-2] == 0 and codes[-1] == 0
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-3, 1.0, 1e4, 1e30])
+def test_weight_magnitudes(scale):
+    w = gaussian_weights(48, 512, seed=9) * scale
+    compare_full(w.to(torch.float32), gaussian_activations(3, 512, seed=10))
+
+
+def test_subnormal_and_mixed_exponent_weights():
+    g = torch.Generator().manual_seed(11)
+    w = torch.randn(40, 256, generator=g) * torch.exp2(torch.randint(-140, 60, (40, 256), generator=g).float())
+    w[0, :8] = torch.tensor([1e-45, -3e-45, 0.0, -0.0, 2e-44, 1e-40, 3e38, -3e38])
+    compare_full(w.to(torch.float32), gaussian_activations(2, 256, seed=12))
+
+
+def test_student_t_weights_and_outlier_tokens():
+    w = student_t_weights(96, 1024, seed=13)
+    x = gaussian_activations(8, 1024, seed=14)
+    x[:, ::97] *= 50
+    compare_full(w, x.to(torch.bfloat16))
+
+
+def test_activation_ties_on_device():
+    # a = 127 exactly, so s = 1 and x*s = x: halves must go to the even integer
+    x = torch.tensor([[2.5, 3.5, -0.5, 126.5, 127.0, -1.5, 0.5, -2.5]], dtype=torch.float32)
+    xq, s = blt.quant_act(x.cuda())
+    assert s.cpu().tolist() == [1.0]
+    assert xq.cpu().tolist() == [[2, 4, 0, 126, 127, -2, 0, -2]]
+
+
+# ------------------------------------------------------------------ invariants of the device path
+def test_pack_is_deterministic_and_order_free():
+    w = gaussian_weights(512, 1024, seed=15)
+    a = blt.pack_weights(w.cuda())
+    b = blt.pack_weights(w.cuda())
+    perm = torch.randperm(w.numel(), generator=torch.Generator().manual_seed(16))
+    c = blt.pack_weights(w.flatten()[perm].reshape(1024, 512).contiguous().cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(a.wp, b.wp) and torch.equal(a.gamma, b.gamma)
+    assert torch.equal(a.gamma, c.gamma)
+
+
+def test_non_default_stream_and_reuse():
+    w = gaussian_weights(256, 512, seed=17)
+    x = gaussian_activations(3, 512, seed=18)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        packed = blt.pack_weights(w.cuda())
+        y1 = blt.forward(x.cuda(), packed)
+        y2 = blt.forward(x.cuda(), packed)
+    s.synchronize()
+    assert torch.equal(y1, y2)
+    ref = oracle.bitlinear_forward(x_to_oracle(x), w.numpy())
+    np.testing.assert_array_equal(bits(y1.cpu().numpy()), bits(ref["y"]))
+
+
+def test_errors_raise_not_fallback():
+    w = gaussian_weights(8, 64, seed=19).cuda()
+    with pytest.raises(blt.BitLinearError):
+        blt.pack_weights(w[:, :62].contiguous())          # K % 4 != 0
+    packed = blt.pack_weights(w)
+    with pytest.raises(ValueError):
+        blt.forward(torch.zeros(2, 60, device="cuda", dtype=torch.bfloat16), packed)
