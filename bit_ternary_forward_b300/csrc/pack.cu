@@ -13,13 +13,18 @@
 // units (below 2^309 for N*K < 2^32); the kernels below compute it without any
 // rounding, in an order-independent way, then divide by N*K and round once.
 //
-//   1. bl_absum_partials: each CTA sums its share of |W| exactly. A thread
-//      keeps a 128-bit accumulator for the 32 binades below (and 4 above) the
-//      CTA's sampled maximum; elements outside that window go to 254
-//      per-exponent 64-bit bins in shared memory. The CTA folds both into a
-//      384-bit fixed-point partial (12 x 32-bit limbs).
-//   2. bl_gamma_finalize: one CTA adds the partials, divides by N*K and rounds
-//      the quotient to fp32, ties to even.
+//   1. bl_absum_partials: each CTA sums its share of |W| exactly. Each warp
+//      picks a window of 32 binades from the largest exponent among its first
+//      128 weights (4 binades above it, 27 below); a lane adds every weight
+//      inside the window, as its 24-bit significand shifted into place, to a
+//      96-bit register accumulator (add with carry); weights outside the
+//      window (zeros, subnormals, stragglers far from the warp's scale) go to
+//      254 per-exponent 64-bit bins in shared memory. The CTA folds both into
+//      a 384-bit fixed-point partial (12 x 32-bit limbs).
+//   2. bl_gamma_finalize: one CTA adds the partials (shuffle reductions), then
+//      one thread divides the top 64 bits of the exact sum by N*K and rounds
+//      the quotient to fp32, ties to even, with the dropped bits and the
+//      remainder as the sticky bit.
 //   3. bl_quant_pack: codes and packing. code = 0 iff |w| <= d/2 with
 //      d = fp32(gamma + 1e-5), which equals clip(rint(fp32(w/d)), -1, 1) for
 //      every finite w (see ternary_field in common.cuh).
@@ -35,43 +40,45 @@ constexpr int kLimbs = 12;            // 384-bit fixed point, units of 2^-149
 constexpr int kSmemLimbs = 16;        // headroom for shifted pieces
 constexpr int kBins = 256;
 
-// |w| = m * 2^e1 in units of 2^-149 (e1 in [0, 253]).
-BL_DEVICE void decompose_abs(float w, uint32_t& m, int& e1) {
-  uint32_t b = __float_as_uint(w) & 0x7fffffffu;
-  uint32_t e = b >> 23;
-  m = (b & 0x7fffffu) | (e ? 0x800000u : 0u);
-  e1 = e ? static_cast<int>(e) - 1 : 0;
+BL_DEVICE float4 ld_stream_f4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
 }
 
-// Adds v * 2^shift to 64-bit shared limbs holding 32 bits of value each.
-BL_DEVICE void add_shifted_u64(unsigned long long* limbs, unsigned long long v, int shift) {
-  if (v == 0) return;
+// (a2:a1:a0) += (hi:lo), 96-bit, carries through the flag register.
+BL_DEVICE void add96(uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t lo, uint32_t hi) {
+  asm("add.cc.u32 %0, %0, %3;\n\t"
+      "addc.cc.u32 %1, %1, %4;\n\t"
+      "addc.u32 %2, %2, 0;"
+      : "+r"(a0), "+r"(a1), "+r"(a2) : "r"(lo), "r"(hi));
+}
+
+BL_DEVICE void add96(uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  asm("add.cc.u32 %0, %0, %3;\n\t"
+      "addc.cc.u32 %1, %1, %4;\n\t"
+      "addc.u32 %2, %2, %5;"
+      : "+r"(a0), "+r"(a1), "+r"(a2) : "r"(b0), "r"(b1), "r"(b2));
+}
+
+// Adds the little-endian 32-bit words w[0..n) times 2^shift to shared limbs
+// that hold 32 bits of value each in 64-bit cells (carries settle later).
+template <int NW>
+BL_DEVICE void add_words_shifted(unsigned long long* limbs, const uint32_t (&w)[NW], int shift) {
   const int q = shift >> 5, r = shift & 31;
-  const uint32_t w[2] = {static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32)};
+  uint32_t prev = 0u;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    unsigned long long piece = static_cast<unsigned long long>(w[i]) << r;   // < 2^63
-    if (piece == 0) continue;
-    atomicAdd(&limbs[q + i], piece & 0xffffffffull);
-    if (piece >> 32) atomicAdd(&limbs[q + i + 1], piece >> 32);
+  for (int i = 0; i <= NW; ++i) {
+    const uint32_t cur = i < NW ? w[i] : 0u;
+    // word i of (w << r): the high half of (cur:prev) << r
+    const uint32_t piece = r ? __funnelshift_l(prev, cur, r) : cur;
+    if (piece) atomicAdd(&limbs[q + i], static_cast<unsigned long long>(piece));
+    prev = cur;
   }
 }
 
-struct Acc128 {
-  unsigned long long lo, hi;
-};
-
-BL_DEVICE void acc_add(Acc128& a, unsigned long long v) {
-  unsigned long long s = a.lo + v;
-  a.hi += (s < a.lo) ? 1ull : 0ull;
-  a.lo = s;
-}
-
-BL_DEVICE void acc_add(Acc128& a, const Acc128& b) {
-  unsigned long long s = a.lo + b.lo;
-  a.hi += b.hi + ((s < a.lo) ? 1ull : 0ull);
-  a.lo = s;
-}
+BL_DEVICE int exp_field(float x) { return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu); }
 
 }  // namespace
 
@@ -79,79 +86,84 @@ __global__ void __launch_bounds__(kAbsumThreads)
 bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials) {
   __shared__ unsigned long long s_bins[kBins];
   __shared__ unsigned long long s_limbs[kSmemLimbs];
-  __shared__ int s_emax;
 
   const int tid = threadIdx.x;
   for (int i = tid; i < kBins; i += blockDim.x) s_bins[i] = 0ull;
   if (tid < kSmemLimbs) s_limbs[tid] = 0ull;
-  if (tid == 0) s_emax = 0;
-  __syncthreads();
 
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   const uint64_t first = static_cast<uint64_t>(blockIdx.x) * blockDim.x + tid;
 
-  // Window base from a sample: the largest exponent among this CTA's first float4s.
-  {
-    int e_loc = 0;
-    if (first < n4) {
-      float4 v = w4[first];
-      uint32_t m; int e1;
-      decompose_abs(v.x, m, e1); e_loc = max(e_loc, e1);
-      decompose_abs(v.y, m, e1); e_loc = max(e_loc, e1);
-      decompose_abs(v.z, m, e1); e_loc = max(e_loc, e1);
-      decompose_abs(v.w, m, e1); e_loc = max(e_loc, e1);
-    }
-    atomicMax(&s_emax, e_loc);
-  }
-  __syncthreads();
-  // window [base, base + 31]: 4 binades above the sample maximum, 27 below
-  const int base = max(0, min(s_emax + 4, 253) - 31);
+  // Warp-uniform window [base, base + 31] in units of 2^-149; a normal weight
+  // with exponent field e and significand m (implicit bit included) is
+  // m * 2^(e - 1) in those units.
+  float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (first < n4) v0 = ld_stream_f4(w4 + first);
+  int e_loc = max(max(exp_field(v0.x), exp_field(v0.y)), max(exp_field(v0.z), exp_field(v0.w)));
+  e_loc = min(e_loc, 254);
+  const int e_max = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(e_loc)));
+  const int top = min(max(e_max - 1, 0) + 4, 253);
+  const int base = max(0, top - 31);
+  const uint32_t bias = static_cast<uint32_t>(base) + 1u;
+  __syncthreads();   // bins and limbs cleared
 
-  Acc128 acc{0ull, 0ull};
+  uint32_t a0 = 0u, a1 = 0u, a2 = 0u;
   auto take = [&](float x) {
-    uint32_t m; int e1;
-    decompose_abs(x, m, e1);
-    const unsigned d = static_cast<unsigned>(e1 - base);
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t e = (b >> 23) & 0xffu;
+    const uint32_t d = e - bias;                      // wraps for e == 0 and below the window
     if (d < 32u) {
-      acc_add(acc, static_cast<unsigned long long>(m) << d);
-    } else if (m) {
-      atomicAdd(&s_bins[e1], static_cast<unsigned long long>(m));
+      const uint32_t m = (b & 0x7fffffu) | 0x800000u;
+      add96(a0, a1, a2, m << d, __funnelshift_l(m, 0u, d));
+    } else if (b & 0x7fffffffu) {
+      const uint32_t m = e ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
+      atomicAdd(&s_bins[e ? e - 1u : 0u], static_cast<unsigned long long>(m));
     }
   };
 
-  uint64_t i = first;
-  for (; i + 3 * stride < n4; i += 4 * stride) {
-    float4 v0 = w4[i], v1 = w4[i + stride], v2 = w4[i + 2 * stride], v3 = w4[i + 3 * stride];
+  if (first < n4) {
     take(v0.x); take(v0.y); take(v0.z); take(v0.w);
-    take(v1.x); take(v1.y); take(v1.z); take(v1.w);
-    take(v2.x); take(v2.y); take(v2.z); take(v2.w);
-    take(v3.x); take(v3.y); take(v3.z); take(v3.w);
+  }
+  uint64_t i = first + stride;
+  for (; i + 3 * stride < n4; i += 4 * stride) {
+    const float4 u0 = ld_stream_f4(w4 + i), u1 = ld_stream_f4(w4 + i + stride);
+    const float4 u2 = ld_stream_f4(w4 + i + 2 * stride), u3 = ld_stream_f4(w4 + i + 3 * stride);
+    take(u0.x); take(u0.y); take(u0.z); take(u0.w);
+    take(u1.x); take(u1.y); take(u1.z); take(u1.w);
+    take(u2.x); take(u2.y); take(u2.z); take(u2.w);
+    take(u3.x); take(u3.y); take(u3.z); take(u3.w);
   }
   for (; i < n4; i += stride) {
-    float4 v = w4[i];
-    take(v.x); take(v.y); take(v.z); take(v.w);
+    const float4 u = ld_stream_f4(w4 + i);
+    take(u.x); take(u.y); take(u.z); take(u.w);
   }
 
-  // warp-reduce the 128-bit window accumulators
+  // warp sum of the 96-bit accumulators (all lanes share `base`)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    Acc128 other;
-    other.lo = __shfl_down_sync(0xffffffffu, acc.lo, o);
-    other.hi = __shfl_down_sync(0xffffffffu, acc.hi, o);
-    acc_add(acc, other);
+    const uint32_t b0 = __shfl_down_sync(0xffffffffu, a0, o);
+    const uint32_t b1 = __shfl_down_sync(0xffffffffu, a1, o);
+    const uint32_t b2 = __shfl_down_sync(0xffffffffu, a2, o);
+    add96(a0, a1, a2, b0, b1, b2);
   }
-  __syncthreads();   // bins complete
+  __syncthreads();   // every bin update done
   if ((tid & 31) == 0) {
-    add_shifted_u64(s_limbs, acc.lo, base);
-    add_shifted_u64(s_limbs, acc.hi, base + 64);
+    const uint32_t w[3] = {a0, a1, a2};
+    add_words_shifted(s_limbs, w, base);
   }
-  for (int e = tid; e < kBins; e += blockDim.x) add_shifted_u64(s_limbs, s_bins[e], e);
+  for (int e = tid; e < kBins; e += blockDim.x) {
+    const unsigned long long v = s_bins[e];
+    if (v) {
+      const uint32_t w[2] = {static_cast<uint32_t>(v), static_cast<uint32_t>(v >> 32)};
+      add_words_shifted(s_limbs, w, e);
+    }
+  }
   __syncthreads();
   if (tid == 0) {
     unsigned long long carry = 0;
     uint32_t* out = partials + static_cast<size_t>(blockIdx.x) * kPartialWords;
     for (int l = 0; l < kLimbs; ++l) {
-      unsigned long long v = s_limbs[l] + carry;
+      const unsigned long long v = s_limbs[l] + carry;
       out[l] = static_cast<uint32_t>(v);
       carry = v >> 32;
     }
@@ -159,82 +171,81 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
   }
 }
 
-namespace {
-
-BL_DEVICE uint32_t get_bit(const uint32_t* q, int pos) { return (q[pos >> 5] >> (pos & 31)) & 1u; }
-
-BL_DEVICE bool any_below(const uint32_t* q, int pos) {   // any bit in [0, pos)
-  const int li = pos >> 5, r = pos & 31;
-  for (int l = 0; l < li; ++l)
-    if (q[l]) return true;
-  return r ? (q[li] & ((1u << r) - 1u)) != 0u : false;
-}
-
-}  // namespace
-
 __global__ void __launch_bounds__(256)
 bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_t count,
                   float* __restrict__ gamma) {
-  __shared__ unsigned long long s_sum[kLimbs];
-  const int tid = threadIdx.x;
-  if (tid < kLimbs) s_sum[tid] = 0ull;
-  __syncthreads();
+  __shared__ unsigned long long s_part[256 / 32][kLimbs];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   unsigned long long loc[kLimbs];
 #pragma unroll
   for (int l = 0; l < kLimbs; ++l) loc[l] = 0ull;
   for (int c = tid; c < n_partials; c += blockDim.x) {
-    const uint32_t* p = partials + static_cast<size_t>(c) * kPartialWords;
-#pragma unroll
-    for (int l = 0; l < kLimbs; ++l) loc[l] += p[l];
+    const uint4* p = reinterpret_cast<const uint4*>(partials + static_cast<size_t>(c) * kPartialWords);
+    const uint4 q0 = p[0], q1 = p[1], q2 = p[2];
+    loc[0] += q0.x; loc[1] += q0.y; loc[2] += q0.z; loc[3] += q0.w;
+    loc[4] += q1.x; loc[5] += q1.y; loc[6] += q1.z; loc[7] += q1.w;
+    loc[8] += q2.x; loc[9] += q2.y; loc[10] += q2.z; loc[11] += q2.w;
   }
 #pragma unroll
-  for (int l = 0; l < kLimbs; ++l)
-    if (loc[l]) atomicAdd(&s_sum[l], loc[l]);
+  for (int l = 0; l < kLimbs; ++l) {
+    unsigned long long v = loc[l];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    if (lane == 0) s_part[warp][l] = v;
+  }
   __syncthreads();
   if (tid != 0) return;
 
-  // normalise the exact sum S into 32-bit limbs (S < 2^309 fits in 10 limbs)
+  // exact sum S in 32-bit limbs (S < 2^309)
   uint32_t S[kLimbs + 1];
   unsigned long long carry = 0;
   for (int l = 0; l < kLimbs; ++l) {
-    unsigned long long v = s_sum[l] + carry;
+    unsigned long long v = carry;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) v += s_part[w][l] & 0xffffffffull;
+    unsigned long long hi = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) hi += s_part[w][l] >> 32;
     S[l] = static_cast<uint32_t>(v);
-    carry = v >> 32;
+    carry = (v >> 32) + hi;
   }
   S[kLimbs] = static_cast<uint32_t>(carry);
 
-  // Q = floor(S / count), R = S mod count (count < 2^32)
-  const unsigned long long D = count;
-  uint32_t Q[kLimbs + 1];
-  unsigned long long rem = 0;
-  for (int l = kLimbs; l >= 0; --l) {
-    unsigned long long cur = (rem << 32) | S[l];
-    Q[l] = static_cast<uint32_t>(cur / D);
-    rem = cur % D;
-  }
-
-  // mean = (Q + rem/D) * 2^-149: round to fp32, ties to even
-  int top = kLimbs;
-  while (top >= 0 && Q[top] == 0u) --top;
-  const int p = top < 0 ? 0 : 32 * top + (32 - __clz(Q[top]));   // bit length of Q
-  const int shift = p > 24 ? p - 24 : 0;
-  uint32_t mant;
+  // T = the top 64 bits of S (all of S when it is shorter), sh = bits dropped
+  int topl = kLimbs;
+  while (topl > 0 && S[topl] == 0u) --topl;
+  const int P = S[topl] ? 32 * topl + (32 - __clz(S[topl])) : 0;   // bit length of S
+  const int sh = P > 64 ? P - 64 : 0;
+  unsigned long long T;
+  bool low_nonzero = false;
   {
-    const int li = shift >> 5, r = shift & 31;
-    unsigned long long two = Q[li];
-    if (li + 1 <= kLimbs) two |= static_cast<unsigned long long>(Q[li + 1]) << 32;
-    mant = static_cast<uint32_t>(two >> r) & 0xffffffu;
+    const int li = sh >> 5, r = sh & 31;
+    const unsigned long long w01 =
+        static_cast<unsigned long long>(S[li]) | (static_cast<unsigned long long>(li + 1 <= kLimbs ? S[li + 1] : 0u) << 32);
+    const uint32_t w2 = li + 2 <= kLimbs ? S[li + 2] : 0u;
+    T = r ? ((w01 >> r) | (static_cast<unsigned long long>(w2) << (64 - r))) : w01;
+    for (int l = 0; l < li; ++l) low_nonzero |= S[l] != 0u;
+    if (r) low_nonzero |= (S[li] & ((1u << r) - 1u)) != 0u;
   }
+  // mean = (q + f) * 2^sh units of 2^-149, f in [0, 1), f > 0 iff rem or low bits
+  const unsigned long long q = T / count;
+  const unsigned long long rem = T - q * count;
+  const int p = q ? 64 - __clzll(static_cast<long long>(q)) : 0;   // bit length of q
+  const int E = p - 1 + sh;                                        // top bit position of the mean
+  const int t = E > 23 ? E - 23 : 0;                               // fp32 spacing 2^t units
+  const int drop = t - sh;                                         // low bits of q to round away
+  unsigned long long mant;
   bool up;
-  if (shift == 0) {
+  if (drop <= 0) {
+    // sh == 0 here: round q + rem/count to an integer
+    mant = q;
     const unsigned long long twice = rem * 2ull;
-    up = twice > D || (twice == D && (mant & 1u));
+    up = twice > count || (twice == count && (q & 1ull));
   } else {
-    const bool guard = get_bit(Q, shift - 1);
-    const bool sticky = any_below(Q, shift - 1) || rem != 0ull;
-    up = guard && (sticky || (mant & 1u));
+    mant = q >> drop;
+    const bool guard = (q >> (drop - 1)) & 1ull;
+    const bool sticky = (drop > 1 && (q & ((1ull << (drop - 1)) - 1ull)) != 0ull) || rem != 0ull || low_nonzero;
+    up = guard && (sticky || (mant & 1ull));
   }
-  unsigned long long bits = (static_cast<unsigned long long>(shift) << 23) + mant + (up ? 1u : 0u);
+  unsigned long long bits = (static_cast<unsigned long long>(t) << 23) + mant + (up ? 1ull : 0ull);
   if (bits >= 0x7f800000ull) bits = 0x7f800000ull;   // unreachable for finite inputs
   *gamma = __uint_as_float(static_cast<uint32_t>(bits));
 }
