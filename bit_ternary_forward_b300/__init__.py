@@ -42,6 +42,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "bitlinear_pack_workspace_bytes": (sz, [i64, i64]),
         "bitlinear_pack_weights": (st, [vp, i64, i64, vp, vp, vp, sz, vp]),
+        "bitlinear_pack_weights_noalloc": (st, [vp, i64, i64, vp, vp, vp]),
         "bitlinear_absmean": (st, [vp, i64, i64, vp, vp, sz, vp]),
         "bitlinear_quantize_pack": (st, [vp, i64, i64, vp, vp, vp]),
         "bitlinear_gemm_workspace_bytes": (sz, [i64, i64, i64]),

@@ -82,6 +82,11 @@ bl_status launch_act_quant(const void* x, bl_dtype dt, int64_t M, int64_t K, int
 
 }  // namespace
 
+namespace bl {
+// Lets entry points defined in other files record their thread-local message.
+bl_status record_error(bl_status st, const char* msg) { return fail(st, "%s", msg); }
+}  // namespace bl
+
 extern "C" {
 
 const char* bitlinear_strerror(bl_status st) {
@@ -121,8 +126,8 @@ bl_status run_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* 
   const uint64_t n4 = nk / 4;
   const int sms = sm_count();
   uint64_t ga = (n4 + bl::kAbsumThreads * 4 - 1) / (bl::kAbsumThreads * 4);
-  const uint64_t cap = static_cast<uint64_t>(sms) * 4 < static_cast<uint64_t>(bl::kMaxAbsumCtas)
-                           ? static_cast<uint64_t>(sms) * 4
+  const uint64_t cap = static_cast<uint64_t>(sms) * 8 < static_cast<uint64_t>(bl::kMaxAbsumCtas)
+                           ? static_cast<uint64_t>(sms) * 8
                            : static_cast<uint64_t>(bl::kMaxAbsumCtas);
   if (ga > cap) ga = cap;
   if (ga < 1) ga = 1;

@@ -4,7 +4,12 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "bitlinear.h"
+
 namespace bl {
+
+// Records `msg` as the calling thread's last error and returns `st` (abi.cu).
+bl_status record_error(bl_status st, const char* msg);
 
 // ---- weight packing (pack.cu)
 constexpr int kAbsumThreads = 256;

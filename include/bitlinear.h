@@ -118,6 +118,32 @@ BL_API bl_status bitlinear_absmean(const float* W, int64_t N, int64_t K, float* 
 BL_API bl_status bitlinear_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma,
                                          uint8_t* Wp, bl_stream_t stream);
 
+/* bitlinear_pack_weights_noalloc: the same packing as bitlinear_pack_weights,
+ * for callers that cannot allocate device memory and so cannot pass a
+ * workspace: a plugin running inside another framework whose caching
+ * allocator owns the device and must not be bypassed, or a runtime that
+ * reserved all device memory up front, where a cudaMalloc would fail or
+ * fragment memory the host framework manages. The pages have no counterpart
+ * of this call; it is an interface convenience.
+ *
+ * Scratch: a static device array of 75,776 bytes (bitlinear_pack_workspace_bytes
+ * of any shape) inside the library, which every GPU that loads the library
+ * holds until the process exits. No cudaMalloc, cudaFree or other allocating
+ * call is made. W, Wp and gamma are as for bitlinear_pack_weights.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture begins. Every call on a device shares the one
+ * array: calls whose work overlaps on the GPU (different streams, no ordering
+ * between them) race and give wrong results; calls ordered on one stream are
+ * safe. Nothing in the array needs to start at zero: each call writes every
+ * slot it reads.
+ *
+ * Returns BL_ERR_UNSUPPORTED (with a message) if the shape needs more scratch
+ * than the array holds, and the statuses of bitlinear_pack_weights otherwise. */
+BL_API bl_status bitlinear_pack_weights_noalloc(const float* W, int64_t N, int64_t K,
+                                                uint8_t* Wp, float* gamma, bl_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * Per-token absmax int8 activation quantisation.
  * Passages: "activation absmax = max(|X|, eps=1e-5)" and per-token 8-bit
