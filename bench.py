@@ -6,8 +6,9 @@ of the workload, with inputs resident in HBM:
 
     a1      bitlinear_absmean        gamma = mean|W| (exact)
     a2-a3   bitlinear_quantize_pack  ternary codes, four per byte
-    a4      bitlinear_quant_act      per-token absmax int8 activations
-    a5-a6   bitlinear_gemm           ternary x int8 contraction + fp32 rescale
+    a4-a6   bitlinear_forward        per-token absmax int8 activations, ternary x
+                                     int8 contraction, fp32 rescale (x_q and s
+                                     are written out too)
 
 The default workload is the 2B-class decode GEMV (M=1, K=2560->N=6912 and
 K=6912->N=2560, fp32 weights packed to 2 bits, bf16 activations). The step
@@ -50,30 +51,36 @@ def row_bytes(p):
     nk, mk, mn = p.n * p.k, p.m * p.k, p.m * p.n
     xb = 2 if p.x_dtype == "bf16" else 4
     return {
-        "absmean": 4 * nk + 4,                          # read W, write gamma
-        "quantize_pack": 4 * nk + nk // 4 + 4,          # read W and gamma, write Wp
-        "quant_act": xb * mk + mk + 4 * p.m,            # read x, write x_q and s
-        "gemm": nk // 4 + mk + 4 * p.m + 4 + 4 * mn,    # read Wp, x_q, s, gamma; write y
+        "absmean": 4 * nk + 4,                                    # read W, write gamma
+        "quantize_pack": 4 * nk + nk // 4 + 4,                    # read W and gamma, write Wp
+        # read x, Wp, gamma; write y and the quantised activations (x_q, s)
+        "forward": xb * mk + nk // 4 + 4 + 4 * mn + mk + 4 * p.m,
     }
 
 
 def row_ops(p):
-    return {"gemm": 2 * p.m * p.n * p.k}
+    return {"forward": 2 * p.m * p.n * p.k}
 
 
-ROWS = ["absmean", "quantize_pack", "quant_act", "gemm"]
-ROW_KERNELS = {
-    "absmean": ["bl_absum_partials", "bl_gamma_finalize"],
-    "quantize_pack": ["bl_quant_pack"],
-    "quant_act": ["bl_act_quant"],
-    "gemm": ["bl_gemv_w2a8"],
-}
+ROWS = ["absmean", "quantize_pack", "forward"]
+FUSED_MAX_M = 8     # the forward quantises activations inside the contraction up to this M
+
+
+def row_kernels(p):
+    if p.k % 64 == 0 and p.m <= 4:
+        fwd = ["bl_gemv_fused"]
+    elif p.k % 64 == 0 and p.m <= FUSED_MAX_M:
+        fwd = ["bl_decode_mma"]
+    else:
+        fwd = ["bl_act_quant", "bl_decode_mma"]
+    return {"absmean": ["bl_absum_partials", "bl_gamma_finalize"], "quantize_pack": ["bl_quant_pack"],
+            "forward": fwd}
 
 
 def workload_units(projs, unit):
     if unit == "GB/s":
         return sum(sum(row_bytes(p).values()) for p in projs)
-    return sum(row_ops(p)["gemm"] for p in projs)
+    return sum(row_ops(p)["forward"] for p in projs)
 
 
 def peaks():
@@ -158,7 +165,7 @@ def traffic_record(kernel_row):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"absmean": "pack.cu", "quantize_pack": "pack.cu", "quant_act": "act_quant.cu", "gemm": "gemv.cu"}[kernel_row]
+    src = {"absmean": "pack.cu", "quantize_pack": "pack.cu", "forward": "gemv_fused.cu"}[kernel_row]
     with open(os.path.join(ROOT, "bit_ternary_forward_b300", "csrc", src), "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()[:16]
     best = None
@@ -256,7 +263,7 @@ class Step:
                     "s": torch.empty(p.m, dtype=torch.float32, device=device),
                     "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device),
                 }
-                nws = max(blt.pack_workspace_bytes(p.n, p.k), int(self.lib.bitlinear_gemm_workspace_bytes(p.m, p.n, p.k)))
+                nws = max(blt.pack_workspace_bytes(p.n, p.k), blt.forward_workspace_bytes(p.m, p.n, p.k))
                 d["ws_t"] = torch.empty(nws + 256, dtype=torch.uint8, device=device)
                 d["ws"] = (d["ws_t"].data_ptr() + 255) // 256 * 256
                 d["nws"] = nws
@@ -280,12 +287,9 @@ class Step:
                                                  d["wp"].data_ptr(), st))
             if events is not None:
                 events.mark(stream)
-            self._ok(lib.bitlinear_quant_act(d["x"].data_ptr(), d["xdt"], p.m, p.k, d["xq"].data_ptr(),
-                                             d["s"].data_ptr(), st))
-            if events is not None:
-                events.mark(stream)
-            self._ok(lib.bitlinear_gemm(d["xq"].data_ptr(), d["s"].data_ptr(), p.m, d["wp"].data_ptr(),
-                                        d["gamma"].data_ptr(), p.n, p.k, d["y"].data_ptr(), d["ws"], d["nws"], st))
+            self._ok(lib.bitlinear_forward(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(), d["gamma"].data_ptr(),
+                                           p.n, p.k, d["y"].data_ptr(), d["xq"].data_ptr(), d["s"].data_ptr(),
+                                           d["ws"], d["nws"], st))
         if events is not None:
             events.mark(stream)
 
@@ -293,7 +297,8 @@ class Step:
         if st != 0:
             raise RuntimeError(self.lib.bitlinear_last_error().decode())
 
-    launches_per_projection = 5   # absum, finalize, quant_pack, act_quant, gemv
+    def launches_per_step(self):
+        return sum(len(k) for p in self.projs for k in row_kernels(p).values())
 
 
 class GraphEvents:
@@ -399,7 +404,7 @@ def main(argv=None):
     while args.steps % G:
         G -= 1
     replays = args.steps // G
-    n_marks = G * (len(projs) * 4 + 1)
+    n_marks = G * (len(projs) * len(ROWS) + 1)
     pool = [torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
     for ev in pool:
         ev.record(stream)
@@ -452,10 +457,11 @@ def main(argv=None):
         avg_ms = tot_ms / launches
         byts = sum(row_bytes(p)[r] for p, _ in per_row[r]) / launches
         gbs = byts / (avg_ms * 1e-3) / 1e9
-        entry = {"row": r, "kernels": ROW_KERNELS[r], "avg_us": 1e3 * avg_ms, "share": None,
+        kern = sorted({k for p, _ in per_row[r] for k in row_kernels(p)[r]})
+        entry = {"row": r, "kernels": kern, "avg_us": 1e3 * avg_ms, "share": None,
                  "bytes_per_launch": byts, "gbs": gbs, "hbm_frac": gbs / hbm}
-        if r == "gemm":
-            ops = sum(row_ops(p)["gemm"] for p, _ in per_row[r]) / launches
+        if r == "forward":
+            ops = sum(row_ops(p)["forward"] for p, _ in per_row[r]) / launches
             entry["tops"] = ops / (avg_ms * 1e-3) / 1e12
         entry["_tot"] = tot_ms
         rows.append(entry)
@@ -463,7 +469,7 @@ def main(argv=None):
     for e in rows:
         e["share"] = e.pop("_tot") / tot_all
     dom = max(rows, key=lambda e: e["share"])
-    if unit == "GB/s" or dom["row"] != "gemm":
+    if unit == "GB/s" or dom["row"] != "forward":
         roof = {"bound": "hbm", "achieved": dom["gbs"], "peak": hbm, "unit": "GB/s", "frac": dom["gbs"] / hbm,
                 "traffic": traffic_record(dom["row"]), "kernel": dom["row"] + " (" + "+".join(dom["kernels"]) + ")",
                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
@@ -480,14 +486,14 @@ def main(argv=None):
         cpu = time_oracle(projs, unit, budget_s=args.cpu_budget)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
-    n_launch = step.launches_per_projection * len(projs) * args.steps
+    n_launch = step.launches_per_step() * args.steps
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8/i8/i32 (f32 scales)", "data": "synthetic (seeded generators)",
         "config": {"workload": wl.name, "description": wl.description,
                    "projections": [f"{p.name}: M={p.m} K={p.k} N={p.n}" for p in projs],
-                   "step": "absmean + quantize_pack + quant_act + gemm per projection",
+                   "step": "absmean + quantize_pack + forward (act quant, contraction, rescale) per projection",
                    "units_per_step": units_step,
                    "l2": f"inputs larger than L2: {args.rotate} rotating input sets of "
                          f"{sum(4 * p.n * p.k + 2 * p.m * p.k for p in projs) / 1e6:.1f} MB",

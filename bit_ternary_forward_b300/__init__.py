@@ -55,6 +55,7 @@ def _load() -> ctypes.CDLL:
         "bitlinear_strerror": (ctypes.c_char_p, [st]),
         "bitlinear_last_error": (ctypes.c_char_p, []),
         "bitlinear_version": (ctypes.c_int, []),
+        "bitlinear_device_error": (st, [ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -240,6 +241,13 @@ def gemm_i32(xq: torch.Tensor, wp: torch.Tensor, acc: Optional[torch.Tensor] = N
     return acc
 
 
-__all__ = ["PackedWeight", "BitLinearError", "pack_weights", "absmean", "quantize_pack", "quant_act", "forward",
+def device_error() -> int:
+    """The device-side error word (non-zero: a kernel gave up a bounded wait); reading clears it."""
+    flag = ctypes.c_int(0)
+    _check("bitlinear_device_error", lib.bitlinear_device_error(ctypes.byref(flag)))
+    return int(flag.value)
+
+
+__all__ = ["device_error", "PackedWeight", "BitLinearError", "pack_weights", "absmean", "quantize_pack", "quant_act", "forward",
            "gemm", "gemm_i32",
            "pack_workspace_bytes", "forward_workspace_bytes", "lib", "LIB_PATH"]

@@ -80,6 +80,54 @@ bl_status launch_act_quant(const void* x, bl_dtype dt, int64_t M, int64_t K, int
   return BL_OK;
 }
 
+// Rows of W per CTA for the mma.sync contraction (bl_decode_mma), or 0 when it
+// does not take this shape (K % 64 != 0, or the shared-memory block is too big).
+int decode_rows(int64_t N, int64_t K) {
+  if (K % 64 != 0) return 0;
+  const int sms = sm_count();
+  int64_t rows = (N + sms - 1) / sms;
+  while (rows > 16 && bl::decode_smem_bytes(static_cast<int>(rows), static_cast<int>(K)) > bl::kMaxSmemPerCta)
+    rows = (rows + 1) / 2;
+  if (bl::decode_smem_bytes(static_cast<int>(rows), static_cast<int>(K)) > bl::kMaxSmemPerCta) return 0;
+  return static_cast<int>(rows);
+}
+
+bl_status launch_decode(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
+                        void* out, bool out_acc, int8_t* xq_out, float* scale_out, int64_t M, int64_t N, int64_t K,
+                        int rows, cudaStream_t s) {
+  cudaError_t e = bl::launch_decode(wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out, static_cast<int>(M),
+                                    static_cast<int>(N), static_cast<int>(K), rows, s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_decode_mma: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
+// Largest M that the forward quantises inside the contraction kernel.
+constexpr int64_t kFusedMaxM = 8;
+
+// Launch plan of the fused dp4a GEMV (M <= 4); smem == 0 when it does not apply.
+struct GemvPlan {
+  int rows = 0, parts = 0;
+  size_t smem = 0;
+};
+
+GemvPlan gemv_plan(int64_t M, int64_t N, int64_t K) {
+  GemvPlan p;
+  if (M > bl::kGemvFusedMaxM) return p;
+  p.smem = bl::gemv_fused_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sm_count(), &p.rows,
+                               &p.parts);
+  return p;
+}
+
+bl_status launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
+                            void* out, bool out_acc, int8_t* xq_out, float* scale_out, int64_t M, int64_t N,
+                            int64_t K, const GemvPlan& p, cudaStream_t s) {
+  cudaError_t e = bl::launch_gemv_fused(wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out,
+                                        static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.rows, p.parts,
+                                        p.smem, s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemv_fused: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
 }  // namespace
 
 namespace bl {
@@ -103,6 +151,17 @@ const char* bitlinear_strerror(bl_status st) {
 const char* bitlinear_last_error(void) { return g_last_error.c_str(); }
 
 int bitlinear_version(void) { return 1; }
+
+bl_status bitlinear_device_error(int* flag) {
+  g_last_error.clear();
+  if (!flag) return fail(BL_ERR_INVALID_ARG, "null pointer (flag)");
+  int a = 0, b = 0;
+  cudaError_t e = bl::take_wait_error(&a);
+  if (e == cudaSuccess) e = bl::take_gemv_wait_error(&b);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bitlinear_device_error: %s", cudaGetErrorString(e));
+  *flag = a | b;
+  return BL_OK;
+}
 
 size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K) {
   (void)N;
@@ -224,7 +283,16 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
   int8_t* xq = xq_out ? xq_out : reinterpret_cast<int8_t*>(ws);
   float* sc = scale_out ? scale_out
                         : reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256));
+  const GemvPlan gp = gemv_plan(M, N, K);
+  if (gp.smem)
+    return launch_gemv_fused(Wp, x, dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32, nullptr, gamma, y, false, xq_out,
+                             scale_out, M, N, K, gp, s);
+  const int rows = decode_rows(N, K);
+  if (rows && M <= kFusedMaxM)
+    return launch_decode(Wp, x, dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32, nullptr, gamma, y, false, xq_out,
+                         scale_out, M, N, K, rows, s);
   if (bl_status st = launch_act_quant(x, dt, M, K, xq, sc, s)) return st;
+  if (rows) return launch_decode(Wp, xq, bl::kXinI8, sc, gamma, y, false, nullptr, nullptr, M, N, K, rows, s);
   return launch_gemv(Wp, xq, sc, gamma, y, M, N, K, bl::GemvOut::kY, s);
 }
 
@@ -244,7 +312,12 @@ bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const 
   if (!xq || !scale || !Wp || !gamma || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (xq, scale, Wp, gamma or y)");
   if (!aligned(xq, 16) || !aligned(Wp, 16) || !aligned(y, 16) || !aligned(scale, 4) || !aligned(gamma, 4))
     return fail(BL_ERR_INVALID_ARG, "xq, Wp and y must be 16-byte aligned, scale and gamma 4-byte aligned");
-  return launch_gemv(Wp, xq, scale, gamma, y, M, N, K, bl::GemvOut::kY, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const GemvPlan gp = gemv_plan(M, N, K);
+  if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, gp, s);
+  if (const int rows = decode_rows(N, K))
+    return launch_decode(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, rows, s);
+  return launch_gemv(Wp, xq, scale, gamma, y, M, N, K, bl::GemvOut::kY, s);
 }
 
 size_t bitlinear_gemm_i32_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -263,8 +336,12 @@ bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp, int64_t M, int
   if (!xq || !Wp || !acc) return fail(BL_ERR_INVALID_ARG, "null pointer (xq, Wp or acc)");
   if (!aligned(xq, 16) || !aligned(Wp, 16) || !aligned(acc, 16))
     return fail(BL_ERR_INVALID_ARG, "xq, Wp and acc must be 16-byte aligned");
-  return launch_gemv(Wp, xq, nullptr, nullptr, acc, M, N, K, bl::GemvOut::kAcc,
-                     reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const GemvPlan gp = gemv_plan(M, N, K);
+  if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, gp, s);
+  if (const int rows = decode_rows(N, K))
+    return launch_decode(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, rows, s);
+  return launch_gemv(Wp, xq, nullptr, nullptr, acc, M, N, K, bl::GemvOut::kAcc, s);
 }
 
 }  // extern "C"

@@ -39,4 +39,35 @@ enum class GemvOut { kY = 0, kAcc = 1 };
 cudaError_t launch_gemv(const uint8_t* wp, const int8_t* xq, const float* scale, const float* gamma, void* out,
                         int M, int N, int K, GemvOut mode, bool vec, int mt, int grid_x, cudaStream_t s);
 
+// ---- decode / skinny contraction on mma.sync (decode.cu)
+constexpr int kDecodeThreads = 512;
+constexpr int kXinF32 = 0, kXinBF16 = 1, kXinI8 = 2;   // activation input kinds
+constexpr size_t kMaxSmemPerCta = 227 * 1024;
+constexpr size_t kOneCtaPerSmSmem = 120 * 1024;   // > half of the 228 KB an SM holds
+
+// Dynamic shared memory of bl_decode_mma for a block of rows_per_cta rows.
+size_t decode_smem_bytes(int rows_per_cta, int K);
+
+// x is fp32 / bf16 (quantised in the kernel; xq_out and scale_out optional) or
+// int8 x_q with scale_in (xin == kXinI8). out is fp32 y or int32 acc [M][N].
+// Needs K % 64 == 0 and 16-byte aligned wp, x.
+cudaError_t launch_decode(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
+                          void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K,
+                          int rows_per_cta, cudaStream_t s);
+
+// Reads and clears the device word set when a bounded wait gave up (synchronous).
+cudaError_t take_wait_error(int* flag);
+
+// ---- decode GEMV for M <= 4 with fused activation quantisation (gemv_fused.cu)
+constexpr int kGemvFusedThreads = 512;
+constexpr int kGemvFusedMaxM = 4;
+// Chooses rows per CTA and the number of k-parts for M x N x K on `sms` SMs;
+// returns the dynamic shared memory in bytes, or 0 if the kernel does not take
+// the shape (M > 4, K % 64 != 0, K too long).
+size_t gemv_fused_plan(int M, int N, int K, int sms, int* rows_per_cta, int* parts);
+cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
+                              void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K,
+                              int rows_per_cta, int parts, size_t smem, cudaStream_t s);
+cudaError_t take_gemv_wait_error(int* flag);
+
 }  // namespace bl

@@ -222,6 +222,12 @@ BL_API const char* bitlinear_strerror(bl_status status);   /* static string */
 BL_API const char* bitlinear_last_error(void);             /* thread-local detail of the last failure */
 BL_API int bitlinear_version(void);                        /* ABI version, currently 1 */
 
+/* Reads and clears the library's device-side error word of the current
+ * device into *flag (host pointer): non-zero if, since the last call, a
+ * kernel gave up a bounded wait for its own asynchronous copies (its outputs
+ * are then unspecified). Synchronises with the device. */
+BL_API bl_status bitlinear_device_error(int* flag);
+
 #ifdef __cplusplus
 }
 #endif

@@ -161,3 +161,9 @@ def test_errors_raise_not_fallback():
     packed = blt.pack_weights(w)
     with pytest.raises(ValueError):
         blt.forward(torch.zeros(2, 60, device="cuda", dtype=torch.bfloat16), packed)
+
+
+def test_no_bounded_wait_gave_up():
+    # every kernel above finished its waits for its own copies in time
+    torch.cuda.synchronize()
+    assert blt.device_error() == 0
