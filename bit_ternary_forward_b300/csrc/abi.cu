@@ -104,6 +104,44 @@ bl_status launch_decode(const uint8_t* wp, const void* x, int xin, const float* 
 // Largest M that the forward quantises inside the contraction kernel.
 constexpr int64_t kFusedMaxM = 8;
 
+bool use_tc(int64_t M, int64_t K) { return M >= bl::kTcMinM && K % 64 == 0; }
+
+// Workspace of the tensor-core path: fp16 operand, token sums, scales.
+struct TcWorkspace {
+  void* xperm;
+  int* rowsum;
+  float* scale;
+};
+
+size_t tc_workspace_bytes(int64_t M, int64_t K) {
+  return align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2, 256) + 2 * align_up(static_cast<size_t>(M) * 4, 256);
+}
+
+TcWorkspace tc_workspace(void* ws, int64_t M, int64_t K) {
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  TcWorkspace t;
+  t.xperm = b;
+  b += align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2, 256);
+  t.rowsum = reinterpret_cast<int*>(b);
+  b += align_up(static_cast<size_t>(M) * 4, 256);
+  t.scale = reinterpret_cast<float*>(b);
+  return t;
+}
+
+bl_status run_tc(const void* x, int xin, const float* scale_in, const uint8_t* Wp, const float* gamma, void* out,
+                 bool out_acc, int8_t* xq_out, float* scale_out, int64_t M, int64_t N, int64_t K, void* ws,
+                 cudaStream_t s) {
+  TcWorkspace t = tc_workspace(ws, M, K);
+  float* sc = xin == bl::kXinI8 ? const_cast<float*>(scale_in) : (scale_out ? scale_out : t.scale);
+  cudaError_t e = bl::launch_act_perm(x, xin, scale_in, static_cast<int>(M), static_cast<int>(K), xq_out,
+                                      xin == bl::kXinI8 ? nullptr : sc, t.xperm, t.rowsum, s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_act_perm: %s", cudaGetErrorString(e));
+  e = bl::launch_gemm_tc(t.xperm, Wp, sc, t.rowsum, gamma, out, out_acc, static_cast<int>(M), static_cast<int>(N),
+                         static_cast<int>(K), s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemm_tc: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
 // Launch plan of the fused dp4a GEMV (M <= 4); smem == 0 when it does not apply.
 struct GemvPlan {
   int rows = 0, parts = 0;
@@ -155,11 +193,12 @@ int bitlinear_version(void) { return 1; }
 bl_status bitlinear_device_error(int* flag) {
   g_last_error.clear();
   if (!flag) return fail(BL_ERR_INVALID_ARG, "null pointer (flag)");
-  int a = 0, b = 0;
+  int a = 0, b = 0, c = 0;
   cudaError_t e = bl::take_wait_error(&a);
   if (e == cudaSuccess) e = bl::take_gemv_wait_error(&b);
+  if (e == cudaSuccess) e = bl::take_tc_wait_error(&c);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bitlinear_device_error: %s", cudaGetErrorString(e));
-  *flag = a | b;
+  *flag = a | b | c;
   return BL_OK;
 }
 
@@ -261,6 +300,7 @@ bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K, 
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   (void)N;
   if (M <= 0 || K <= 0) return 0;
+  if (use_tc(M, K)) return tc_workspace_bytes(M, K);
   return align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) + align_up(static_cast<size_t>(M) * 4, 256);
 }
 
@@ -283,10 +323,11 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
   int8_t* xq = xq_out ? xq_out : reinterpret_cast<int8_t*>(ws);
   float* sc = scale_out ? scale_out
                         : reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256));
+  const int xin = dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32;
+  if (use_tc(M, K)) return run_tc(x, xin, nullptr, Wp, gamma, y, false, xq_out, scale_out, M, N, K, workspace, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem)
-    return launch_gemv_fused(Wp, x, dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32, nullptr, gamma, y, false, xq_out,
-                             scale_out, M, N, K, gp, s);
+    return launch_gemv_fused(Wp, x, xin, nullptr, gamma, y, false, xq_out, scale_out, M, N, K, gp, s);
   const int rows = decode_rows(N, K);
   if (rows && M <= kFusedMaxM)
     return launch_decode(Wp, x, dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32, nullptr, gamma, y, false, xq_out,
@@ -297,22 +338,22 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
 }
 
 size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)M;
   (void)N;
-  (void)K;
-  return 0;
+  return (M > 0 && K > 0 && use_tc(M, K)) ? tc_workspace_bytes(M, K) : 0;
 }
 
 bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const uint8_t* Wp, const float* gamma,
                          int64_t N, int64_t K, float* y, void* workspace, size_t ws_bytes, bl_stream_t stream) {
   g_last_error.clear();
-  (void)workspace;
-  (void)ws_bytes;
   if (bl_status st = check_dims(M, N, K, true)) return st;
   if (!xq || !scale || !Wp || !gamma || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (xq, scale, Wp, gamma or y)");
   if (!aligned(xq, 16) || !aligned(Wp, 16) || !aligned(y, 16) || !aligned(scale, 4) || !aligned(gamma, 4))
     return fail(BL_ERR_INVALID_ARG, "xq, Wp and y must be 16-byte aligned, scale and gamma 4-byte aligned");
+  const size_t need = bitlinear_gemm_workspace_bytes(M, N, K);
+  if (need && (!workspace || !aligned(workspace, 256) || ws_bytes < need))
+    return fail(BL_ERR_WORKSPACE, "gemm workspace needs %zu bytes, 256-byte aligned", need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc(M, K)) return run_tc(xq, bl::kXinI8, scale, Wp, gamma, y, false, nullptr, nullptr, M, N, K, workspace, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, gp, s);
   if (const int rows = decode_rows(N, K))
@@ -321,22 +362,21 @@ bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const 
 }
 
 size_t bitlinear_gemm_i32_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)M;
-  (void)N;
-  (void)K;
-  return 0;
+  return bitlinear_gemm_workspace_bytes(M, N, K);
 }
 
 bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp, int64_t M, int64_t N, int64_t K, int32_t* acc,
                              void* workspace, size_t ws_bytes, bl_stream_t stream) {
   g_last_error.clear();
-  (void)workspace;
-  (void)ws_bytes;
   if (bl_status st = check_dims(M, N, K, true)) return st;
   if (!xq || !Wp || !acc) return fail(BL_ERR_INVALID_ARG, "null pointer (xq, Wp or acc)");
   if (!aligned(xq, 16) || !aligned(Wp, 16) || !aligned(acc, 16))
     return fail(BL_ERR_INVALID_ARG, "xq, Wp and acc must be 16-byte aligned");
+  const size_t need = bitlinear_gemm_i32_workspace_bytes(M, N, K);
+  if (need && (!workspace || !aligned(workspace, 256) || ws_bytes < need))
+    return fail(BL_ERR_WORKSPACE, "gemm_i32 workspace needs %zu bytes, 256-byte aligned", need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (use_tc(M, K)) return run_tc(xq, bl::kXinI8, nullptr, Wp, nullptr, acc, true, nullptr, nullptr, M, N, K, workspace, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, gp, s);
   if (const int rows = decode_rows(N, K))

@@ -70,4 +70,18 @@ cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const f
                               int rows_per_cta, int parts, size_t smem, cudaStream_t s);
 cudaError_t take_gemv_wait_error(int* flag);
 
+// ---- prefill contraction on tcgen05 (prefill.cu)
+constexpr int kTcMinM = 65;   // smallest M routed to the tensor-core kernel
+size_t gemm_tc_smem_bytes();
+// x (fp32 / bf16, or int8 x_q with xin == kXinI8) -> fp16 operand xperm [M][K]
+// (transposed 16-code blocks scaled by 4^-i), token sums rowsum [M], and for
+// float input the scales scale_out [M] and optionally int8 codes xq_out.
+cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M, int K, int8_t* xq_out,
+                            float* scale_out, void* xperm, int* rowsum, cudaStream_t s);
+// y (or int32 acc when out_acc) from xperm, rowsum, scale and packed weights;
+// needs K % 64 == 0. Returns cudaErrorNotSupported if tensor maps cannot be made.
+cudaError_t launch_gemm_tc(const void* xperm, const uint8_t* wp, const float* scale, const int* rowsum,
+                           const float* gamma, void* out, bool out_acc, int M, int N, int K, cudaStream_t s);
+cudaError_t take_tc_wait_error(int* flag);
+
 }  // namespace bl

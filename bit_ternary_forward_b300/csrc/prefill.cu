@@ -1,0 +1,663 @@
+// Prefill contraction on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Passages: "穿越1比特的奇幻旅程" (2B4T summary), section "GPU端：CUDA内核的定制
+// 魔法" (W1.58A8 matmul over four-per-byte packed weights: pack, store, load,
+// unpack, compute); "BitNet 1-bit LLM 的混合精度微调技术：渐进量化策略", body,
+// quantisation functions and forward-pass sentence (per-token absmax int8
+// activations, rescale by the factors).
+//
+// sm_103a has no integer kind for tcgen05.mma, so the contraction runs as
+// kind::f16 (fp16 x fp16 -> fp32) and is made exact:
+//
+//   * Weights. A packed byte holds the fields f = code + 1 of k = 4j .. 4j+3
+//     at bits 2i. Spreading two bytes of a word into the low bytes of two
+//     16-bit lanes and masking plane i (0x0003 << 2i) leaves 4^i * f in each
+//     lane; read as an fp16 bit pattern that is the subnormal 4^i * f * 2^-24.
+//     Two byte permutes and eight masks expand 16 codes.
+//   * Activations. The matching slot holds x_q * 4^-i, also exact in fp16
+//     (|x_q| <= 127, 4^-i >= 2^-6). Slot 16q + 4i + j of a 64-wide k-stage
+//     stands for k = 16q + 4j + i: within each 16-code block the activations
+//     are stored transposed as a 4 x 4 matrix, matching the plane order.
+//   * Every product is then f * x_q * 2^-24 exactly, and every partial sum is
+//     an integer times 2^-24 of magnitude at most 2 * 127 * K * 2^-24 < 1 for
+//     K <= 65536, so the fp32 accumulator holds it exactly (as long as the
+//     tensor core adds integers below 2^24 without loss, which the GPU parity
+//     tests check bit for bit). The epilogue scales by 2^24,
+//     subtracts the token sum of x_q (field = code + 1) and applies
+//     y = fp32(fp32(acc * gamma) / s).
+//
+// Kernel shape: persistent, one CTA per SM, tiles of 128 weight rows x BN
+// tokens (BN chosen per shape from 128..256 so the tiles spread evenly over
+// the SMs), 448 threads:
+//   warp 0      TMA producer: activation tile [BN][64] fp16 (128-byte
+//               swizzle) and packed weight tile [128][16] bytes per stage,
+//               as many stages as fit (5 at BN = 256, 10 at BN = 128: about
+//               the latency-bandwidth product of one SM's share of L2);
+//   warp 1      allocates 512 TMEM columns (two accumulators) and issues
+//               tcgen05.mma (M = 128 weight rows, N = BN tokens, K = 16)
+//               from one thread;
+//   warps 2..9  expand each packed stage into the fp16 operand, canonical
+//               128-byte-swizzled K-major layout, in a separate three-deep
+//               ring (half a row per thread);
+//   warps 10..13 epilogue of the previous tile while the MMA fills the other
+//               accumulator: tcgen05.ld 32x32b (TMEM lane = weight row, one
+//               lane quarter per warp), stores coalesced along the rows.
+// Every wait on the full / expanded / empty stage barriers and on the
+// accumulator barriers is bounded.
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace bl {
+
+namespace {
+
+constexpr int kBM = 128;                    // weight rows per tile: the MMA's M
+constexpr int kBK = 64;                     // k per stage (one 128-byte fp16 swizzle atom)
+constexpr int kEStages = 3;                 // expanded-weight ring
+constexpr int kThreads = 448;
+constexpr int kMaxBN = 256;                 // tokens per tile at most: the MMA's N
+constexpr int kMaxStages = 10;
+constexpr uint32_t kTmemCols = 512;         // two accumulators of up to 256 columns
+constexpr uint32_t kWpBytes = kBM * kBK / 4;    // 2048
+constexpr uint32_t kWeBytes = kBM * kBK * 2;    // 16384
+// barriers (256 B), then per-token epilogue data for two tiles: scale,
+// reciprocal, token sum (fp32) and per-chunk flags
+constexpr uint32_t kEpiBytes = 3 * kMaxBN * 4 + 64;
+constexpr uint32_t kMiscBytes = 256 + 2 * kEpiBytes;
+constexpr uint32_t kSmemBudget = 232448;    // opt-in shared memory per CTA
+// TMA stage: activation tile [BN][64] fp16, then packed weights [128][16] bytes
+// (a multiple of 1024 bytes, so every swizzled tile stays 1024-aligned).
+constexpr uint32_t stage_bytes(int bn) { return static_cast<uint32_t>(bn) * kBK * 2 + kWpBytes; }
+// As many TMA stages as fit: the ring should hold about one latency's worth
+// of the SM's operand stream whatever the tile width.
+constexpr int stages_for(int bn) {
+  return static_cast<int>((kSmemBudget - 1024 - kEStages * kWeBytes - kMiscBytes) / stage_bytes(bn)) < kMaxStages
+             ? static_cast<int>((kSmemBudget - 1024 - kEStages * kWeBytes - kMiscBytes) / stage_bytes(bn))
+             : kMaxStages;
+}
+constexpr uint32_t smem_for(int bn) {
+  return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + kEStages * kWeBytes + kMiscBytes + 1024;
+}
+constexpr uint32_t kWaitTries = 1u << 16;
+
+__device__ int g_tc_wait_error;
+
+BL_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+BL_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+BL_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+BL_DEVICE void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// One bounded-time wait: the hardware suspends the thread until the phase
+// completes or a system-dependent time limit passes.
+BL_DEVICE bool mbar_try(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait: true once the phase completed, false after kWaitTries
+// suspended waits (each ends by itself), so a lost arrival cannot hang.
+BL_DEVICE bool mbar_wait(uint64_t* bar, uint32_t phase) {
+  for (uint32_t i = 0; i < kWaitTries; ++i)
+    if (mbar_try(bar, phase)) return true;
+  return false;
+}
+
+BL_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout: 128-byte rows, 8-row groups 1024 bytes apart.
+BL_DEVICE uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3fffu);          // start address
+  d |= static_cast<uint64_t>(1u) << 16;                        // leading byte offset (unused for this layout)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                // stride byte offset: 8-row group pitch
+  d |= static_cast<uint64_t>(1u) << 46;                        // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both
+// K-major, M = 128, N = BN.
+template <int BN>
+constexpr uint32_t idesc_f16() {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+template <int BN>
+BL_DEVICE void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc_f16<BN>()), "r"(accumulate)
+      : "memory");
+}
+
+BL_DEVICE void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+BL_DEVICE void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+BL_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+BL_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+BL_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// fp32(t / s) rounded to nearest even, from the reciprocal r = fp32(1/s):
+// Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): with q = RN(t * r) within an ulp of t/s, the residual t - q*s is
+// exact in one FMA and q + residual * r, rounded once, is the correctly
+// rounded quotient. The theorem assumes no underflow or overflow, so the
+// caller takes this path only for |t| and s within 2^-96 .. 2^96 and uses
+// the IEEE division otherwise.
+BL_DEVICE float div_rn_markstein(float t, float s, float r) {
+  const float q = __fmul_rn(t, r);
+  const float e = __fmaf_rn(-q, s, t);
+  return __fmaf_rn(e, r, q);
+}
+
+}  // namespace
+
+template <int BN, bool OUT_ACC>
+__global__ void __launch_bounds__(kThreads, 1)
+bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+           const float* __restrict__ scale, const int* __restrict__ rowsum, const float* __restrict__ gamma,
+           void* __restrict__ out, int M, int N, int K) {
+  constexpr int kStages = stages_for(BN);
+  constexpr uint32_t kStageBytes = stage_bytes(BN);
+  constexpr uint32_t kXBytes = static_cast<uint32_t>(BN) * kBK * 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* we_base = smem + kStages * kStageBytes;               // expanded weights, 1024-aligned
+  uint8_t* misc = we_base + kEStages * kWeBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(misc);            // TMA stage landed
+  uint64_t* empty = full + kStages;                              // TMA stage consumed by the MMA
+  uint64_t* expd = empty + kStages;                              // expanded buffer ready
+  uint64_t* efree = expd + kEStages;                             // expanded buffer consumed
+  uint64_t* tfull = efree + kEStages;                            // accumulator b holds a finished tile
+  uint64_t* tempty = tfull + 2;                                  // accumulator b has been read out
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_tiles_n = (N + kBM - 1) / kBM;
+  const int n_tiles = n_tiles_n * ((M + BN - 1) / BN);
+  const int k_iters = K / kBK;
+  bool ok = true;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int e = 0; e < kEStages; ++e) {
+      mbar_init(&expd[e], 8);
+      mbar_init(&efree[e], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---- TMA producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
+        for (int it = 0; it < k_iters; ++it, ++g) {
+          const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+          if (g >= kStages) ok = mbar_wait(&empty[s], ph ^ 1u) && ok;
+          uint8_t* st = smem + s * kStageBytes;
+          mbar_expect_tx(&full[s], kXBytes + kWpBytes);
+          tma_load_2d(st, &tm_x, it * kBK, m0, &full[s]);
+          tma_load_2d(st + kXBytes, &tm_w, it * (kBK / 4), n0, &full[s]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0, tcount = 0;
+      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
+        const uint32_t b = tcount & 1u;
+        if (tcount >= 2) ok = mbar_wait(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
+        tc_fence_after();
+        const uint32_t d = tmem + b * 256u;
+        for (int it = 0; it < k_iters; ++it, ++g) {
+          const uint32_t s = g % kStages, e = g % kEStages, eph = (g / kEStages) & 1u;
+          ok = mbar_wait(&expd[e], eph) && ok;   // also means TMA stage s has landed
+          tc_fence_after();
+          const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes));   // activations [BN][64]
+          const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_f16<BN>(d, adesc + 2u * kk, bdesc + 2u * kk, (it | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit(&efree[e]);
+        }
+        umma_commit(&tfull[b]);
+      }
+    }
+  } else if (warp < 10) {
+    // ---- weight expansion: thread t expands half h = t / 128 (32 codes) of
+    // row r = t % 128 of each stage
+    const int t = tid - 64;
+    const int r = t & (kBM - 1), h = t >> 7;
+    const uint32_t sw = static_cast<uint32_t>(r & 7);
+    uint32_t g = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      for (int it = 0; it < k_iters; ++it, ++g) {
+        const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+        const uint32_t e = g % kEStages, eph = (g / kEStages) & 1u;
+        ok = mbar_wait(&full[s], ph) && ok;
+        if (g >= kEStages) ok = mbar_wait(&efree[e], eph ^ 1u) && ok;
+        const uint2 pw = *reinterpret_cast<const uint2*>(smem + s * kStageBytes + kXBytes + r * 16 + h * 8);
+        uint8_t* row = we_base + e * kWeBytes + r * 128;
+        const uint32_t words[2] = {pw.x, pw.y};
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const uint32_t q = static_cast<uint32_t>(2 * h + qq);
+          const uint32_t lo = __byte_perm(words[qq], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
+          const uint32_t hi = __byte_perm(words[qq], 0u, 0x4342);   // bytes 2, 3
+          const uint4 c0 = make_uint4(lo & 0x00030003u, hi & 0x00030003u, lo & 0x000c000cu, hi & 0x000c000cu);
+          const uint4 c1 = make_uint4(lo & 0x00300030u, hi & 0x00300030u, lo & 0x00c000c0u, hi & 0x00c000c0u);
+          *reinterpret_cast<uint4*>(row + (((2u * q) ^ sw) << 4)) = c0;
+          *reinterpret_cast<uint4*>(row + (((2u * q + 1u) ^ sw) << 4)) = c1;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&expd[e]);
+      }
+    }
+  } else {
+    // ---- epilogue: TMEM lane = weight row, column = token.
+    // D = (sum_k field * x_q) * 2^-24 exactly; every value below is an
+    // integer smaller than 2^24 in magnitude, so the fp32 arithmetic is exact
+    // up to the rescale, which rounds as fp32(fp32(acc * gamma) / s).
+    // The reciprocal-and-correction division needs |t| = |acc * gamma| and s
+    // inside 2^-96..2^96: for gamma inside 2^-72..2^72 every nonzero |t| is
+    // (|acc| <= 127 * 65536), so the choice is made per 32-token chunk, which
+    // keeps the common path free of branches.
+    const int et = tid - 320;                    // 0..127
+    const int quarter = warp & 3;
+    const float gm = OUT_ACC ? 0.f : __ldg(gamma);
+    const bool gamma_fast = OUT_ACC || (gm > 0x1p-72f && gm < 0x1p72f);
+    uint32_t tcount = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
+      const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
+      const uint32_t b = tcount & 1u;
+      float* s_scale = reinterpret_cast<float*>(misc + 256 + b * kEpiBytes);
+      float* s_rcp = s_scale + kMaxBN;           // fp32(1/s), or 0 where the IEEE division must be used
+      float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q as (exact) fp32
+      int* s_fast = reinterpret_cast<int*>(s_rowsum + kMaxBN);   // per 32-token chunk: all reciprocals usable
+      for (int i = et; i < BN; i += 128) {
+        const int m = m0 + i;
+        const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
+        s_scale[i] = sc;
+        s_rcp[i] = (sc > 0x1p-96f && sc < 0x1p96f) ? __frcp_rn(sc) : 0.f;
+        s_rowsum[i] = static_cast<float>(m < M ? __ldg(rowsum + m) : 0);   // |sum| <= 127 K < 2^24: exact
+      }
+      for (int c = warp - 10; c < BN / 32; c += 4) {
+        const int m = m0 + c * 32 + lane;
+        const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
+        const unsigned all = __ballot_sync(0xffffffffu, OUT_ACC || (sc > 0x1p-96f && sc < 0x1p96f));
+        if (lane == 0) s_fast[c] = all == 0xffffffffu;
+      }
+      named_bar(1, 128);                         // the per-token data is complete
+      ok = mbar_wait(&tfull[b], (tcount >> 1) & 1u) && ok;
+      tc_fence_after();
+      const int n = n0 + quarter * 32 + lane;
+      float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
+      int32_t* arow = OUT_ACC ? static_cast<int32_t*>(out) + static_cast<size_t>(m0) * N + n : nullptr;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + b * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+        if (n >= N) continue;
+        const bool full_chunk = m0 + c0 + 32 <= M;
+        if (full_chunk && gamma_fast && s_fast[c0 >> 5]) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float acc = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.f), s_rowsum[c0 + j]);
+            const size_t o = static_cast<size_t>(c0 + j) * N;
+            if constexpr (OUT_ACC) {
+              arow[o] = static_cast<int>(acc);
+            } else {
+              yrow[o] = div_rn_markstein(__fmul_rn(acc, gm), s_scale[c0 + j], s_rcp[c0 + j]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (m0 + c0 + j < M) {
+              const float acc = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.f), s_rowsum[c0 + j]);
+              const size_t o = static_cast<size_t>(c0 + j) * N;
+              if constexpr (OUT_ACC) {
+                arow[o] = static_cast<int>(acc);
+              } else {
+                const float t = __fmul_rn(acc, gm);
+                const float at = fabsf(t);
+                const float rr = s_rcp[c0 + j];
+                yrow[o] = (rr != 0.f && (at == 0.f || (at > 0x1p-96f && at < 0x1p96f)))
+                              ? div_rn_markstein(t, s_scale[c0 + j], rr)
+                              : __fdiv_rn(t, s_scale[c0 + j]);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (!ok) atomicExch(&g_tc_wait_error, 1);
+}
+
+// Per-token activation pass for the tensor-core path: the scale, optional
+// int8 codes, the token sum of the codes, and the fp16 operand (transposed
+// 16-code blocks, slot 16q + 4i + j = x_q[16q + 4j + i] * 4^-i).
+template <int XIN>
+__global__ void __launch_bounds__(256)
+bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int K, int8_t* __restrict__ xq_out,
+            float* __restrict__ scale_out, __half* __restrict__ xperm, int* __restrict__ rowsum) {
+  __shared__ float s_red[8];
+  __shared__ int s_sum[8];
+  const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nblk = K >> 4;
+  float s = 1.f;
+  if constexpr (XIN != kXinI8) {
+    float amax = 0.f;
+    for (int b = tid; b < nblk; b += blockDim.x) {
+      float f[16];
+      if constexpr (XIN == kXinF32) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + static_cast<size_t>(m) * K) + 4 * b;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldg(p + i);
+          f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
+        }
+      } else {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + static_cast<size_t>(m) * K) + 2 * b;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint4 v = __ldg(p + i);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+            f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) s_red[warp] = amax;
+    __syncthreads();
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) a = fmaxf(a, s_red[w]);
+    s = token_scale(a);
+    if (tid == 0 && scale_out) scale_out[m] = s;
+  }
+  int part = 0;
+  for (int b = tid; b < nblk; b += blockDim.x) {
+    int q[16];
+    if constexpr (XIN == kXinI8) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const int8_t*>(x) + static_cast<size_t>(m) * K) + b);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) q[j] = static_cast<int>(static_cast<int8_t>((u[j >> 2] >> (8 * (j & 3))) & 0xffu));
+    } else {
+      float f[16];
+      if constexpr (XIN == kXinF32) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + static_cast<size_t>(m) * K) + 4 * b;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldg(p + i);
+          f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
+        }
+      } else {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + static_cast<size_t>(m) * K) + 2 * b;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint4 v = __ldg(p + i);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+            f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) q[j] = quant_code(f[j], s);
+      if (xq_out) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w[i] = (static_cast<uint32_t>(q[4 * i]) & 0xffu) | ((static_cast<uint32_t>(q[4 * i + 1]) & 0xffu) << 8) |
+                 ((static_cast<uint32_t>(q[4 * i + 2]) & 0xffu) << 16) | ((static_cast<uint32_t>(q[4 * i + 3]) & 0xffu) << 24);
+        *reinterpret_cast<uint4*>(xq_out + static_cast<size_t>(m) * K + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    // slot 4i + j holds x_q[4j + i] * 4^-i (exact in fp16)
+    __half h[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float sc = i == 0 ? 1.f : (i == 1 ? 0.25f : (i == 2 ? 0.0625f : 0.015625f));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[4 * i + j] = __float2half_rn(static_cast<float>(q[4 * j + i]) * sc);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) part += q[j];
+    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<size_t>(m) * K + 16 * b);
+    dst[0] = *reinterpret_cast<const uint4*>(&h[0]);
+    dst[1] = *reinterpret_cast<const uint4*>(&h[8]);
+  }
+  part = warp_sum(part);
+  if (lane == 0) s_sum[warp] = part;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t += s_sum[w];
+    rowsum[m] = t;
+  }
+}
+
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+size_t gemm_tc_smem_bytes() { return smem_for(kMaxBN); }
+
+namespace {
+
+// Token-tile width: the one whose tiles, dealt round-robin to the SMs, finish
+// first. A k-stage costs nearly the same for narrow tiles (the per-stage
+// issue work of the MMA thread, not the tensor pipe, sets its length there),
+// so a tile's time is taken as proportional to max(BN, 200); ties go to the
+// wider tile.
+int pick_bn(int M, int N, int sms) {
+  const int cands[5] = {256, 224, 192, 160, 128};
+  int best = 256;
+  long long best_cost = -1;
+  const int tn = (N + kBM - 1) / kBM;
+  for (int bn : cands) {
+    const long long tiles = static_cast<long long>(tn) * ((M + bn - 1) / bn);
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long cost = waves * (bn > 200 ? bn : 200);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <int BN, bool OUT_ACC>
+cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale, const int* rowsum,
+                        const float* gamma, void* out, int M, int N, int K, int sms, cudaStream_t s) {
+  static size_t done = 0;
+  constexpr size_t smem = smem_for(BN);
+  static_assert(smem <= kSmemBudget, "shared memory budget");
+  static_assert(stages_for(BN) >= 4, "pipeline depth");
+  if (done < smem) {
+    cudaError_t e = cudaFuncSetAttribute(bl_gemm_tc<BN, OUT_ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    done = smem;
+  }
+  const int tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  const int grid = tiles < sms ? tiles : sms;
+  bl_gemm_tc<BN, OUT_ACC><<<grid, kThreads, smem, s>>>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K);
+  return cudaGetLastError();
+}
+
+template <bool OUT_ACC>
+cudaError_t launch_tc_bn(int bn, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale,
+                         const int* rowsum, const float* gamma, void* out, int M, int N, int K, int sms,
+                         cudaStream_t s) {
+  switch (bn) {
+    case 224: return launch_tc_t<224, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+    case 192: return launch_tc_t<192, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+    case 160: return launch_tc_t<160, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+    case 128: return launch_tc_t<128, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+    default: return launch_tc_t<256, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M, int K, int8_t* xq_out,
+                            float* scale_out, void* xperm, int* rowsum, cudaStream_t s) {
+  __half* xp = static_cast<__half*>(xperm);
+  if (xin == kXinF32)
+    bl_act_perm<kXinF32><<<M, 256, 0, s>>>(x, scale_in, K, xq_out, scale_out, xp, rowsum);
+  else if (xin == kXinBF16)
+    bl_act_perm<kXinBF16><<<M, 256, 0, s>>>(x, scale_in, K, xq_out, scale_out, xp, rowsum);
+  else
+    bl_act_perm<kXinI8><<<M, 256, 0, s>>>(x, scale_in, K, xq_out, scale_out, xp, rowsum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const void* xperm, const uint8_t* wp, const float* scale, const int* rowsum,
+                           const float* gamma, void* out, bool out_acc, int M, int N, int K, cudaStream_t s) {
+  EncodeTiled enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 148;
+  const int bn = pick_bn(M, N, sms);
+  CUtensorMap tm_x, tm_w;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {kBK, static_cast<cuuint32_t>(bn)};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(xperm), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 4), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 4)};
+    const cuuint32_t box[2] = {kBK / 4, kBM};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wp), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (out_acc) return launch_tc_bn<true>(bn, tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+  return launch_tc_bn<false>(bn, tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+}
+
+cudaError_t take_tc_wait_error(int* flag) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_tc_wait_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_tc_wait_error, &zero, sizeof(int));
+}
+
+}  // namespace bl

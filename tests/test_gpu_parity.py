@@ -163,6 +163,29 @@ def test_errors_raise_not_fallback():
         blt.forward(torch.zeros(2, 60, device="cuda", dtype=torch.bfloat16), packed)
 
 
+@pytest.mark.parametrize("gexp", [-40, -8, 0, 20])
+def test_tensor_core_rescale_bit_exact_over_scale_range(gexp):
+    # the tensor-core epilogue divides with a reciprocal and one correction
+    # step inside 2^-96..2^96 and with IEEE division outside; both must give
+    # fp32(fp32(acc * gamma) / s) bit for bit over every scale 127/max(|x|,
+    # 1e-5) can take (about 3.7e-37 .. 1.27e7)
+    rng = np.random.default_rng(200 + gexp)
+    m, n, k = 2048, 256, 128
+    xq = rng.integers(-127, 128, size=(m, k)).astype(np.int8)
+    codes = rng.integers(-1, 2, size=(n, k)).astype(np.int8)
+    s = (10.0 ** rng.uniform(-36.4, 7.1, size=m)).astype(np.float32)
+    gamma = np.float32(rng.uniform(1.0, 2.0) * 2.0 ** gexp)
+    packed = blt.PackedWeight(torch.from_numpy(oracle.pack_codes(codes)).cuda(),
+                              torch.tensor([gamma], dtype=torch.float32).cuda(), n, k)
+    y = blt.gemm(torch.from_numpy(xq).cuda(), torch.from_numpy(s).cuda(), packed)
+    acc = blt.gemm_i32(torch.from_numpy(xq).cuda(), packed.wp)
+    torch.cuda.synchronize()
+    acc_ref = oracle.ternary_int8_matmul(xq, codes)
+    np.testing.assert_array_equal(acc.cpu().numpy(), acc_ref)
+    y_ref = oracle.rescale(acc_ref, gamma, s)
+    np.testing.assert_array_equal(bits(y.cpu().numpy()), bits(y_ref))
+
+
 def test_no_bounded_wait_gave_up():
     # every kernel above finished its waits for its own copies in time
     torch.cuda.synchronize()
