@@ -79,9 +79,10 @@ def row_kernels(p):
             "forward": fwd}
 
 
-def workload_units(projs, unit):
+def workload_units(projs, unit, rows=None):
+    rows = rows or ROWS
     if unit == "GB/s":
-        return sum(sum(row_bytes(p).values()) for p in projs)
+        return sum(sum(v for r, v in row_bytes(p).items() if r in rows) for p in projs)
     return sum(row_ops(p)["forward"] for p in projs)
 
 
@@ -181,15 +182,20 @@ def traffic_record(kernel_row, prefill=False):
 
 
 # --------------------------------------------------------------------------- oracle (CPU) timing
-def oracle_step(inputs, rows_per_proj):
+def oracle_step(inputs, rows_per_proj, pack=True):
+    """One oracle step on the first rows_per_proj weight rows of each projection.
+    With pack=False the codes come from the set-up (packed once, reused)."""
     import oracle
     done = 0
-    for (w, x, p) in inputs:
+    for (w, x, p, pre) in inputs:
         n = min(rows_per_proj, p.n)
-        wn = w[:n]
-        g = oracle.absmean_gamma(wn)
-        c = oracle.ternary_codes(wn, g)
-        oracle.pack_codes(c)
+        if pack:
+            wn = w[:n]
+            g = oracle.absmean_gamma(wn)
+            c = oracle.ternary_codes(wn, g)
+            oracle.pack_codes(c)
+        else:
+            g, c = pre[0], pre[1][:n]
         xq, s = oracle.quant_act(x)
         acc = oracle.ternary_int8_matmul(xq, c)
         oracle.rescale(acc, g, s)
@@ -197,7 +203,7 @@ def oracle_step(inputs, rows_per_proj):
     return done
 
 
-def oracle_inputs(projs):
+def oracle_inputs(projs, pack=True):
     import oracle
     out = []
     for p in projs:
@@ -206,89 +212,113 @@ def oracle_inputs(projs):
             xf = oracle.bf16_bits_to_f32(x.view(torch.int16).numpy().view(np.uint16))
         else:
             xf = x.numpy()
-        out.append((w.numpy(), xf, p))
+        wn = w.numpy()
+        pre = None
+        if not pack:
+            g = oracle.absmean_gamma(wn)
+            pre = (g, oracle.ternary_codes(wn, g))
+        out.append((wn, xf, p, pre))
     return out
 
 
-def sampled_units(projs, rows, unit):
+def sampled_units(projs, n_rows, unit, rows=None):
     tot = 0
     for p in projs:
-        n = min(rows, p.n)
+        n = min(n_rows, p.n)
         q = type(p)(p.name, p.m, p.k, n, p.w_seed, p.x_seed, p.w_dist, p.x_dist, p.x_dtype)
-        tot += workload_units([q], unit)
+        tot += workload_units([q], unit, rows)
     return tot
 
 
-def time_oracle(projs, unit, budget_s, steps=None, warmup=0):
-    """Oracle throughput on a row sample sized so that `steps` steps take about budget_s."""
-    inputs = oracle_inputs(projs)
+def time_oracle(projs, unit, budget_s, steps=None, warmup=0, rows=None):
+    """Oracle throughput on a row sample sized so that `steps` steps take about budget_s.
+    rows: the bench rows the step covers (without the packing rows the codes
+    are made once before timing, as the packed-once workloads do)."""
+    pack = rows is None or "absmean" in rows
+    inputs = oracle_inputs(projs, pack)
     t = time.perf_counter()
-    oracle_step(inputs, 64)
+    oracle_step(inputs, 64, pack)
     t64 = max(time.perf_counter() - t, 1e-3)
     n_steps = steps if steps else 1
-    rows = int(64 * (budget_s / n_steps) / t64)
-    rows = max(1, min(rows, max(p.n for p in projs)))
+    n_rows = int(64 * (budget_s / n_steps) / t64)
+    n_rows = max(1, min(n_rows, max(p.n for p in projs)))
     for _ in range(warmup):
-        oracle_step(inputs, rows)
+        oracle_step(inputs, n_rows, pack)
     t = time.perf_counter()
     for _ in range(n_steps):
-        oracle_step(inputs, rows)
+        oracle_step(inputs, n_rows, pack)
     el = time.perf_counter() - t
-    units = sampled_units(projs, rows, unit) * n_steps
+    units = sampled_units(projs, n_rows, unit, rows) * n_steps
     scale = 1e9 if unit == "GB/s" else 1e12
     return {"value": units / el / scale, "unit": unit, "cores": 1, "kind": "oracle", "seconds": el,
             "steps": n_steps,
-            "sample": f"first {rows} weight rows of each projection (all tokens), {n_steps} step(s); "
-                      f"numpy oracle, single thread"}
+            "sample": f"first {n_rows} weight rows of each of {len(projs)} projection(s) (all tokens), "
+                      f"{n_steps} step(s); numpy oracle, single thread"}
 
 
 # --------------------------------------------------------------------------- the GPU step
 class Step:
-    def __init__(self, projs, device, rotate):
+    """The timed step. Single-projection workloads pack weights inside the step
+    (absmean, quantize_pack, forward); the 7B-class stacks pack every layer
+    once at set-up and reuse it, so their step is the forward of every
+    projection."""
+
+    def __init__(self, projs, device, rotate, pack_in_step=True):
         import bit_ternary_forward_b300 as blt
+        from workloads.synth import gaussian_activations_on, student_t_weights_on
         self.blt = blt
         self.lib = blt.lib
         self.projs = projs
         self.device = device
+        self.pack_in_step = pack_in_step
+        self.rows = ROWS if pack_in_step else ["forward"]
         self.slots = []
         for r in range(rotate):
             slot = []
             for p in projs:
-                w, x = make_projection_inputs(p)
-                if r:
-                    w = w.clone()
+                nws = max(blt.pack_workspace_bytes(p.n, p.k), blt.forward_workspace_bytes(p.m, p.n, p.k))
                 d = {
                     "p": p,
-                    "w": w.to(device),
-                    "x": x.to(device),
                     "gamma": torch.empty(1, dtype=torch.float32, device=device),
                     "wp": torch.empty((p.n, p.k // 4), dtype=torch.uint8, device=device),
                     "xq": torch.empty((p.m, p.k), dtype=torch.int8, device=device),
                     "s": torch.empty(p.m, dtype=torch.float32, device=device),
                     "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device),
+                    "ws_t": torch.empty(nws + 256, dtype=torch.uint8, device=device),
+                    "nws": nws,
                 }
-                nws = max(blt.pack_workspace_bytes(p.n, p.k), blt.forward_workspace_bytes(p.m, p.n, p.k))
-                d["ws_t"] = torch.empty(nws + 256, dtype=torch.uint8, device=device)
                 d["ws"] = (d["ws_t"].data_ptr() + 255) // 256 * 256
-                d["nws"] = nws
-                d["xdt"] = blt.BL_BF16 if x.dtype == torch.bfloat16 else blt.BL_F32
+                if pack_in_step:
+                    w, x = make_projection_inputs(p)
+                    d["w"] = (w.clone() if r else w).to(device)
+                    d["x"] = x.to(device)
+                else:
+                    w = student_t_weights_on(device, p.n, p.k, p.w_seed) if p.w_dist == "t4" else \
+                        make_projection_inputs(p)[0].to(device)
+                    blt.pack_weights(w, out=blt.PackedWeight(d["wp"], d["gamma"], p.n, p.k))
+                    torch.cuda.synchronize(device)
+                    del w
+                    d["x"] = gaussian_activations_on(device, p.m, p.k, p.x_seed + 7919 * r)
+                d["xdt"] = blt.BL_BF16 if d["x"].dtype == torch.bfloat16 else blt.BL_F32
                 slot.append(d)
             self.slots.append(slot)
         self.rotate = rotate
 
     def run(self, i, stream, events=None):
-        """One step on rotation slot i; events (list) receives external event records between calls."""
+        """One step on rotation slot i; events receives external event records between calls."""
         lib = self.lib
         st = stream.cuda_stream
         for d in self.slots[i % self.rotate]:
             p = d["p"]
-            if events is not None:
-                events.mark(stream)
-            self._ok(lib.bitlinear_absmean(d["w"].data_ptr(), p.n, p.k, d["gamma"].data_ptr(), d["ws"], d["nws"], st))
-            if events is not None:
-                events.mark(stream)
-            self._ok(lib.bitlinear_quantize_pack(d["w"].data_ptr(), p.n, p.k, d["gamma"].data_ptr(),
-                                                 d["wp"].data_ptr(), st))
+            if self.pack_in_step:
+                if events is not None:
+                    events.mark(stream)
+                self._ok(lib.bitlinear_absmean(d["w"].data_ptr(), p.n, p.k, d["gamma"].data_ptr(), d["ws"], d["nws"],
+                                               st))
+                if events is not None:
+                    events.mark(stream)
+                self._ok(lib.bitlinear_quantize_pack(d["w"].data_ptr(), p.n, p.k, d["gamma"].data_ptr(),
+                                                     d["wp"].data_ptr(), st))
             if events is not None:
                 events.mark(stream)
             self._ok(lib.bitlinear_forward(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(), d["gamma"].data_ptr(),
@@ -302,7 +332,7 @@ class Step:
             raise RuntimeError(self.lib.bitlinear_last_error().decode())
 
     def launches_per_step(self):
-        return sum(len(k) for p in self.projs for k in row_kernels(p).values())
+        return sum(len(k) for p in self.projs for r, k in row_kernels(p).items() if r in self.rows)
 
 
 class GraphEvents:
@@ -356,7 +386,9 @@ def run_reference(args, world, rank):
     wl = WORKLOADS[args.workload]
     projs = wl.projections if wl.layers == 1 else wl.projections[:4]
     unit = "GB/s" if args.unit == "GB/s" else "TOPS"
-    r = time_oracle(projs, unit, budget_s=args.reference_budget, steps=args.steps, warmup=min(args.warmup, 3))
+    rows = ROWS if wl.layers == 1 else ["forward"]
+    r = time_oracle(projs, unit, budget_s=args.reference_budget, steps=args.steps, warmup=min(args.warmup, 3),
+                    rows=rows)
     line = {"metric": METRIC, "impl": "reference", "value": r["value"], "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r["seconds"] / r["steps"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f32",
@@ -393,7 +425,9 @@ def main(argv=None):
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     projs = wl.projections
-    step = Step(projs, device, args.rotate)
+    pack_in_step = wl.layers == 1
+    step = Step(projs, device, args.rotate if pack_in_step else 1, pack_in_step)
+    rows_used = step.rows
     stream = torch.cuda.Stream(device)
     hbm, bf16, bf16_sus, peak_src = peaks()
 
@@ -408,7 +442,7 @@ def main(argv=None):
     while args.steps % G:
         G -= 1
     replays = args.steps // G
-    n_marks = G * (len(projs) * len(ROWS) + 1)
+    n_marks = G * (len(projs) * len(rows_used) + 1)
     pool = [torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
     for ev in pool:
         ev.record(stream)
@@ -441,21 +475,21 @@ def main(argv=None):
     ms = max_over_ranks(ms, world, device)
 
     # per-call device times from the last replay's external events
-    per_row = {r: [] for r in ROWS}
-    marks_per_step = len(projs) * len(ROWS) + 1
+    per_row = {r: [] for r in rows_used}
+    marks_per_step = len(projs) * len(rows_used) + 1
     for i in range(G):
         k = i * marks_per_step
         for p in projs:
-            for r in ROWS:
+            for r in rows_used:
                 per_row[r].append((p, pool[k].elapsed_time(pool[k + 1])))
                 k += 1
     unit = args.unit
     scale = 1e9 if unit == "GB/s" else 1e12
-    units_step = workload_units(projs, unit)
+    units_step = workload_units(projs, unit, rows_used)
     value = world * units_step * args.steps / (ms * 1e-3) / scale
 
     rows = []
-    for r in ROWS:
+    for r in rows_used:
         tot_ms = sum(t for _, t in per_row[r])
         launches = len(per_row[r])
         avg_ms = tot_ms / launches
@@ -489,7 +523,8 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(projs, unit, budget_s=args.cpu_budget)
+        cpu = time_oracle(projs if pack_in_step else projs[:4], unit, budget_s=args.cpu_budget,
+                          rows=rows_used)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     n_launch = step.launches_per_step() * args.steps
@@ -520,22 +555,30 @@ def main(argv=None):
 
 
 def run_e2e(step, projs, device, stream, steps, unit, scale):
-    """Host-resident inputs: H2D copies, the public API calls and a D2H of y, every step."""
+    """Host-resident inputs: H2D copies, the public API calls and a D2H of y, every step.
+
+    With packing in the step the fp32 weights are inputs too (copied and packed
+    every step); for the packed-once stacks the packed weights stay resident
+    as model state and only the activations travel."""
     import bit_ternary_forward_b300 as blt
     host = []
-    for p in projs:
-        w, x = make_projection_inputs(p)
-        host.append((p, w.pin_memory(), x.pin_memory(), torch.empty((p.m, p.n), dtype=torch.float32).pin_memory()))
-    dev = [(torch.empty((p.n, p.k), dtype=torch.float32, device=device),
-            torch.empty((p.m, p.k), dtype=hx.dtype, device=device)) for p, _, hx, _ in host]
-    h2d = sum(hw.numel() * 4 + hx.numel() * hx.element_size() for _, hw, hx, _ in host)
-    d2h = sum(hy.numel() * 4 for _, _, _, hy in host)
+    for p, d in zip(projs, step.slots[0]):
+        hx = d["x"].cpu().pin_memory()
+        hw = d["w"].cpu().pin_memory() if step.pack_in_step else None
+        host.append((p, d, hw, hx, torch.empty((p.m, p.n), dtype=torch.float32).pin_memory()))
+    dev = [(torch.empty((p.n, p.k), dtype=torch.float32, device=device) if hw is not None else None,
+            torch.empty((p.m, p.k), dtype=hx.dtype, device=device)) for p, _, hw, hx, _ in host]
+    h2d = sum((hw.numel() * 4 if hw is not None else 0) + hx.numel() * hx.element_size() for _, _, hw, hx, _ in host)
+    d2h = sum(hy.numel() * 4 for _, _, _, _, hy in host)
 
     def one():
-        for (p, hw, hx, hy), (dw, dx) in zip(host, dev):
-            dw.copy_(hw, non_blocking=True)
+        for (p, d, hw, hx, hy), (dw, dx) in zip(host, dev):
             dx.copy_(hx, non_blocking=True)
-            packed = blt.pack_weights(dw)
+            if hw is not None:
+                dw.copy_(hw, non_blocking=True)
+                packed = blt.pack_weights(dw)
+            else:
+                packed = blt.PackedWeight(d["wp"], d["gamma"], p.n, p.k)
             y = blt.forward(dx, packed)
             hy.copy_(y, non_blocking=True)
 
@@ -551,9 +594,11 @@ def run_e2e(step, projs, device, stream, steps, unit, scale):
         t1.record(stream)
     stream.synchronize()
     ms = t0.elapsed_time(t1)
-    return {"value": workload_units(projs, unit) * steps / (ms * 1e-3) / scale, "unit": unit,
+    rows = step.rows
+    return {"value": workload_units(projs, unit, rows) * steps / (ms * 1e-3) / scale, "unit": unit,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "api": "bit_ternary_forward_b300.pack_weights + forward, pinned host buffers"}
+            "api": "bit_ternary_forward_b300." + ("pack_weights + forward" if step.pack_in_step else "forward") +
+                   ", pinned host buffers"}
 
 
 if __name__ == "__main__":

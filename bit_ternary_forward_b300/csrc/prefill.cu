@@ -416,115 +416,155 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // Per-token activation pass for the tensor-core path: the scale, optional
 // int8 codes, the token sum of the codes, and the fp16 operand (transposed
 // 16-code blocks, slot 16q + 4i + j = x_q[16q + 4j + i] * 4^-i).
-template <int XIN>
-__global__ void __launch_bounds__(256)
-bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int K, int8_t* __restrict__ xq_out,
-            float* __restrict__ scale_out, __half* __restrict__ xperm, int* __restrict__ rowsum) {
-  __shared__ float s_red[8];
-  __shared__ int s_sum[8];
-  const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nblk = K >> 4;
-  float s = 1.f;
-  if constexpr (XIN != kXinI8) {
-    float amax = 0.f;
-    for (int b = tid; b < nblk; b += blockDim.x) {
-      float f[16];
-      if constexpr (XIN == kXinF32) {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + static_cast<size_t>(m) * K) + 4 * b;
+//
+// One warp per token, eight tokens per CTA. Lane l takes 16-code blocks l,
+// l + 32, ...; the first kCache of them stay in registers between the absmax
+// reduction (warp shuffles only) and the quantisation. Codes are rounded
+// with the 1.5 * 2^23 addition (exact round-to-nearest-even for |v| <= 2^22
+// after the clamp), which also leaves the code in the low mantissa byte.
+namespace {
+
+constexpr int kPermCache = 4;                // 16-code blocks per lane kept in registers
+
+// Raw 16-activation block: 2 (bf16) or 4 (fp32) 16-byte vectors.
+template <int XIN> struct Raw16 {
+  static constexpr int kVec = XIN == kXinF32 ? 4 : 2;
+  uint4 v[kVec];
+  BL_DEVICE void load(const void* x, size_t off) {
+    const uint4* p = XIN == kXinF32 ? reinterpret_cast<const uint4*>(static_cast<const float*>(x) + off)
+                                    : reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = __ldg(p + i);
-          f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
-        }
-      } else {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + static_cast<size_t>(m) * K) + 2 * b;
+    for (int i = 0; i < kVec; ++i) v[i] = __ldg(p + i);
+  }
+  BL_DEVICE void widen(float (&f)[16]) const {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint4 v = __ldg(p + i);
-          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int i = 0; i < kVec; ++i) {
+      const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
-            f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
-          }
+      for (int j = 0; j < 4; ++j) {
+        if constexpr (XIN == kXinF32) {
+          f[4 * i + j] = __uint_as_float(u[j]);
+        } else {
+          f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+          f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
         }
       }
+    }
+  }
+};
+
+// Codes of one 16-block (fp32 integers q[j] in -128..127 and packed int8
+// words) and its fp16 operand block.
+BL_DEVICE void emit_block(const float (&q)[16], int8_t* xq_row, __half* xp_row, int b, bool write_xq, int& sum) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t b0 = __float_as_uint(__fadd_rn(q[4 * i], 12582912.f));
+    const uint32_t b1 = __float_as_uint(__fadd_rn(q[4 * i + 1], 12582912.f));
+    const uint32_t b2 = __float_as_uint(__fadd_rn(q[4 * i + 2], 12582912.f));
+    const uint32_t b3 = __float_as_uint(__fadd_rn(q[4 * i + 3], 12582912.f));
+    w[i] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+  }
+  if (write_xq) *reinterpret_cast<uint4*>(xq_row + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+  sum = dp4a_ss(static_cast<int>(w[0]), 0x01010101, sum);
+  sum = dp4a_ss(static_cast<int>(w[1]), 0x01010101, sum);
+  sum = dp4a_ss(static_cast<int>(w[2]), 0x01010101, sum);
+  sum = dp4a_ss(static_cast<int>(w[3]), 0x01010101, sum);
+  // slot 4i + j holds x_q[4j + i] * 4^-i (exact: small integers times powers of two)
+  uint32_t h[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float sc = i == 0 ? 1.f : (i == 1 ? 0.25f : (i == 2 ? 0.0625f : 0.015625f));
+    const __half2 lo = __floats2half2_rn(__fmul_rn(q[i], sc), __fmul_rn(q[4 + i], sc));
+    const __half2 hi = __floats2half2_rn(__fmul_rn(q[8 + i], sc), __fmul_rn(q[12 + i], sc));
+    h[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
+    h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(xp_row + 16 * b);
+  dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// fp32 integer value of the code of x: clip(rint(fp32(x * s)), -128, 127).
+BL_DEVICE float code_f(float x, float s) {
+  const float v = fminf(fmaxf(__fmul_rn(x, s), -128.f), 127.f);
+  return __fsub_rn(__fadd_rn(v, 12582912.f), 12582912.f);
+}
+
+}  // namespace
+
+template <int XIN>
+__global__ void __launch_bounds__(256)
+bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int M, int K,
+            int8_t* __restrict__ xq_out, float* __restrict__ scale_out, __half* __restrict__ xperm,
+            int* __restrict__ rowsum) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int nblk = K >> 4;
+  const size_t row = static_cast<size_t>(m) * K;
+  __half* xp_row = xperm + row;
+  int sum = 0;
+  if constexpr (XIN == kXinI8) {
+    const int8_t* xr = static_cast<const int8_t*>(x) + row;
+    for (int b = lane; b < nblk; b += 32) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + b);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      float q[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        q[j] = static_cast<float>(static_cast<int8_t>((u[j >> 2] >> (8 * (j & 3))) & 0xffu));
+      emit_block(q, nullptr, xp_row, b, false, sum);
+    }
+  } else {
+    Raw16<XIN> cache[kPermCache];
+    float amax = 0.f;
+#pragma unroll
+    for (int c = 0; c < kPermCache; ++c) {
+      const int b = lane + 32 * c;
+      if (b < nblk) {
+        cache[c].load(x, row + 16 * b);
+        float f[16];
+        cache[c].widen(f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      }
+    }
+    for (int b = lane + 32 * kPermCache; b < nblk; b += 32) {
+      Raw16<XIN> r;
+      r.load(x, row + 16 * b);
+      float f[16];
+      r.widen(f);
 #pragma unroll
       for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
     }
     amax = warp_max(amax);
-    if (lane == 0) s_red[warp] = amax;
-    __syncthreads();
-    float a = 0.f;
+    const float s = token_scale(amax);
+    if (lane == 0 && scale_out) scale_out[m] = s;
+    int8_t* xq_row = xq_out ? xq_out + row : nullptr;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) a = fmaxf(a, s_red[w]);
-    s = token_scale(a);
-    if (tid == 0 && scale_out) scale_out[m] = s;
-  }
-  int part = 0;
-  for (int b = tid; b < nblk; b += blockDim.x) {
-    int q[16];
-    if constexpr (XIN == kXinI8) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const int8_t*>(x) + static_cast<size_t>(m) * K) + b);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int c = 0; c < kPermCache; ++c) {
+      const int b = lane + 32 * c;
+      if (b < nblk) {
+        float f[16], q[16];
+        cache[c].widen(f);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) q[j] = static_cast<int>(static_cast<int8_t>((u[j >> 2] >> (8 * (j & 3))) & 0xffu));
-    } else {
-      float f[16];
-      if constexpr (XIN == kXinF32) {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + static_cast<size_t>(m) * K) + 4 * b;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = __ldg(p + i);
-          f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
-        }
-      } else {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + static_cast<size_t>(m) * K) + 2 * b;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const uint4 v = __ldg(p + i);
-          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
-            f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) q[j] = quant_code(f[j], s);
-      if (xq_out) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          w[i] = (static_cast<uint32_t>(q[4 * i]) & 0xffu) | ((static_cast<uint32_t>(q[4 * i + 1]) & 0xffu) << 8) |
-                 ((static_cast<uint32_t>(q[4 * i + 2]) & 0xffu) << 16) | ((static_cast<uint32_t>(q[4 * i + 3]) & 0xffu) << 24);
-        *reinterpret_cast<uint4*>(xq_out + static_cast<size_t>(m) * K + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < 16; ++j) q[j] = code_f(f[j], s);
+        emit_block(q, xq_row, xp_row, b, xq_out != nullptr, sum);
       }
     }
-    // slot 4i + j holds x_q[4j + i] * 4^-i (exact in fp16)
-    __half h[16];
+    for (int b = lane + 32 * kPermCache; b < nblk; b += 32) {
+      Raw16<XIN> r;
+      r.load(x, row + 16 * b);
+      float f[16], q[16];
+      r.widen(f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float sc = i == 0 ? 1.f : (i == 1 ? 0.25f : (i == 2 ? 0.0625f : 0.015625f));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) h[4 * i + j] = __float2half_rn(static_cast<float>(q[4 * j + i]) * sc);
+      for (int j = 0; j < 16; ++j) q[j] = code_f(f[j], s);
+      emit_block(q, xq_row, xp_row, b, xq_out != nullptr, sum);
     }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) part += q[j];
-    uint4* dst = reinterpret_cast<uint4*>(xperm + static_cast<size_t>(m) * K + 16 * b);
-    dst[0] = *reinterpret_cast<const uint4*>(&h[0]);
-    dst[1] = *reinterpret_cast<const uint4*>(&h[8]);
   }
-  part = warp_sum(part);
-  if (lane == 0) s_sum[warp] = part;
-  __syncthreads();
-  if (tid == 0) {
-    int t = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) t += s_sum[w];
-    rowsum[m] = t;
-  }
+  sum = warp_sum(sum);
+  if (lane == 0) rowsum[m] = sum;
 }
 
 namespace {
@@ -611,12 +651,13 @@ cudaError_t launch_tc_bn(int bn, const CUtensorMap& tm_x, const CUtensorMap& tm_
 cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M, int K, int8_t* xq_out,
                             float* scale_out, void* xperm, int* rowsum, cudaStream_t s) {
   __half* xp = static_cast<__half*>(xperm);
+  const int grid = (M + 7) / 8;
   if (xin == kXinF32)
-    bl_act_perm<kXinF32><<<M, 256, 0, s>>>(x, scale_in, K, xq_out, scale_out, xp, rowsum);
+    bl_act_perm<kXinF32><<<grid, 256, 0, s>>>(x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
   else if (xin == kXinBF16)
-    bl_act_perm<kXinBF16><<<M, 256, 0, s>>>(x, scale_in, K, xq_out, scale_out, xp, rowsum);
+    bl_act_perm<kXinBF16><<<grid, 256, 0, s>>>(x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
   else
-    bl_act_perm<kXinI8><<<M, 256, 0, s>>>(x, scale_in, K, xq_out, scale_out, xp, rowsum);
+    bl_act_perm<kXinI8><<<grid, 256, 0, s>>>(x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
   return cudaGetLastError();
 }
 

@@ -47,6 +47,26 @@ def student_t_weights(n: int, k: int, seed: int, nu: int = 4, std: float = WEIGH
     return (t * std).to(torch.float32).contiguous()
 
 
+def student_t_weights_on(device, n: int, k: int, seed: int, nu: int = 4, std: float = WEIGHT_STD) -> torch.Tensor:
+    """The Student-t recipe drawn by a seeded generator on ``device`` (fast for
+    multi-GB weight stacks; same distribution, different draws from the CPU
+    generator, so only for timing)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    z = torch.randn((n, k), generator=g, dtype=torch.float32, device=device)
+    v = torch.zeros((n, k), dtype=torch.float32, device=device)
+    for _ in range(nu):
+        v += torch.randn((n, k), generator=g, dtype=torch.float32, device=device) ** 2
+    return (z / torch.sqrt(v / nu) * std).contiguous()
+
+
+def gaussian_activations_on(device, m: int, k: int, seed: int, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """x ~ N(0, 1) drawn by a seeded generator on ``device``, then cast (timing only)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return torch.randn((m, k), generator=g, dtype=torch.float32, device=device).to(dtype).contiguous()
+
+
 def gaussian_activations(m: int, k: int, seed: int, dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
     """x ~ N(0, 1) drawn in fp32, then cast to ``dtype``."""
     x = torch.randn((m, k), generator=_gen(seed), dtype=torch.float32)
