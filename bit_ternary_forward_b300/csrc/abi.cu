@@ -106,6 +106,12 @@ constexpr int64_t kFusedMaxM = 8;
 
 bool use_tc(int64_t M, int64_t K) { return M >= bl::kTcMinM && K % 64 == 0; }
 
+// Workspace of the CUDA-core paths: int8 codes (caller layout or transposed
+// blocks) [M][K], then int token sums [M], then fp32 scales [M].
+size_t small_workspace_bytes(int64_t M, int64_t K) {
+  return align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) + 2 * align_up(static_cast<size_t>(M) * 4, 256);
+}
+
 // Workspace of the tensor-core path: fp16 operand, token sums, scales.
 struct TcWorkspace {
   void* xperm;
@@ -158,10 +164,10 @@ GemvPlan gemv_plan(int64_t M, int64_t N, int64_t K) {
 
 bl_status launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
                             void* out, bool out_acc, int8_t* xq_out, float* scale_out, int64_t M, int64_t N,
-                            int64_t K, const GemvPlan& p, cudaStream_t s) {
+                            int64_t K, const GemvPlan& p, void* workspace, cudaStream_t s) {
   cudaError_t e = bl::launch_gemv_fused(wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out,
                                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.rows, p.parts,
-                                        p.smem, s);
+                                        p.smem, workspace, s);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemv_fused: %s", cudaGetErrorString(e));
   return BL_OK;
 }
@@ -301,7 +307,7 @@ size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   (void)N;
   if (M <= 0 || K <= 0) return 0;
   if (use_tc(M, K)) return tc_workspace_bytes(M, K);
-  return align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) + align_up(static_cast<size_t>(M) * 4, 256);
+  return small_workspace_bytes(M, K);
 }
 
 bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t* Wp, const float* gamma,
@@ -327,7 +333,7 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
   if (use_tc(M, K)) return run_tc(x, xin, nullptr, Wp, gamma, y, false, xq_out, scale_out, M, N, K, workspace, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem)
-    return launch_gemv_fused(Wp, x, xin, nullptr, gamma, y, false, xq_out, scale_out, M, N, K, gp, s);
+    return launch_gemv_fused(Wp, x, xin, nullptr, gamma, y, false, xq_out, scale_out, M, N, K, gp, workspace, s);
   const int rows = decode_rows(N, K);
   if (rows && M <= kFusedMaxM)
     return launch_decode(Wp, x, dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32, nullptr, gamma, y, false, xq_out,
@@ -338,8 +344,10 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
 }
 
 size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
-  return (M > 0 && K > 0 && use_tc(M, K)) ? tc_workspace_bytes(M, K) : 0;
+  if (M <= 0 || K <= 0) return 0;
+  if (use_tc(M, K)) return tc_workspace_bytes(M, K);
+  if (gemv_plan(M, N, K).smem) return small_workspace_bytes(M, K);
+  return 0;
 }
 
 bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const uint8_t* Wp, const float* gamma,
@@ -355,7 +363,7 @@ bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc(M, K)) return run_tc(xq, bl::kXinI8, scale, Wp, gamma, y, false, nullptr, nullptr, M, N, K, workspace, s);
   const GemvPlan gp = gemv_plan(M, N, K);
-  if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, gp, s);
+  if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, gp, workspace, s);
   if (const int rows = decode_rows(N, K))
     return launch_decode(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, rows, s);
   return launch_gemv(Wp, xq, scale, gamma, y, M, N, K, bl::GemvOut::kY, s);
@@ -378,7 +386,7 @@ bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp, int64_t M, int
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc(M, K)) return run_tc(xq, bl::kXinI8, nullptr, Wp, nullptr, acc, true, nullptr, nullptr, M, N, K, workspace, s);
   const GemvPlan gp = gemv_plan(M, N, K);
-  if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, gp, s);
+  if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, gp, workspace, s);
   if (const int rows = decode_rows(N, K))
     return launch_decode(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, rows, s);
   return launch_gemv(Wp, xq, nullptr, nullptr, acc, M, N, K, bl::GemvOut::kAcc, s);

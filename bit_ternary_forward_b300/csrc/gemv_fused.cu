@@ -1,5 +1,6 @@
-// Decode GEMV for one to four tokens: activation quantisation fused with the
-// packed-ternary x int8 contraction, on dp4a.
+// Decode GEMV for one to four tokens: a per-token activation kernel and a
+// packed-ternary x int8 contraction on dp4a, chained with programmatic
+// dependent launch.
 //
 // Passages: "穿越1比特的奇幻旅程" (2B4T summary), section "GPU端：CUDA内核的定制
 // 魔法" (W1.58A8 matmul over four-per-byte packed weights: pack, store, load,
@@ -8,27 +9,36 @@
 // sentence (multiply back by the factors).
 //
 // At M <= 4 the work is one stream of the packed weights (N*K/4 bytes) against
-// a few KB of activations, and a 2B-class projection (4.4 MB) lasts about as
-// long as one HBM round trip, so the kernel is shaped to have as few serial
-// phases as possible:
-//   1. On entry every warp issues the loads of all its weight words straight
-//      into registers (L1-bypassing 4-byte loads, 128 contiguous bytes per
-//      warp instruction): the CTA's whole row block is in flight at once.
-//   2. Meanwhile the CTA reads x once (kept in registers), reduces the
-//      per-token absmax (warp shuffles, one block barrier), quantises and
-//      stages the codes in shared memory with each 16-code block transposed
-//      as a 4x4 byte matrix, plus the per-token code sums (a second barrier).
-//   3. Each warp owns whole rows of one k-part (the row length is split into
-//      P parts only when a lane's share would not fit in registers). Lane l
-//      takes words l, l + 32, ... of the part; it loads the matching
-//      activation words once and keeps them across all its rows. A packed
-//      word masked into its four field planes, (word & 0x03030303 << 2i), is
-//      multiplied by word i of the transposed activation block with dp4a:
+// a few KB of activations; a 2B-class projection (4.4 MB) lasts about as long
+// as one HBM round trip, so the path is shaped to overlap everything with
+// that round trip:
+//   1. bl_act_tq (one CTA per token) quantises x once: scale s, optional
+//      int8 codes in the caller's layout, the token sum of the codes, and the
+//      codes again with each 16-code block transposed as a 4x4 byte matrix
+//      (word i of a block holds the codes of k = 16b + 4j + i, j = 0..3).
+//      Both kernels are launched as programmatic dependents: each first waits
+//      for the grid before it (griddepcontrol.wait) and only then lets its
+//      own dependent start, so a kernel can be resident before its
+//      predecessor ends, while no early read can overtake a write of any
+//      kernel but the one it waits for.
+//   2. bl_gemv_w starts while (1) runs: every warp issues the loads of all its
+//      weight words straight into registers (L1-bypassing, 128 contiguous
+//      bytes per warp instruction), and only then waits for (1). The weights
+//      are never written by (1), and (1) let this grid start only after its
+//      own wait, so the early loads see every earlier write; everything (1)
+//      writes is read after the wait.
+//   3. Each warp owns whole rows of one k-part (the row is split into P parts
+//      only when a lane's share would not fit in registers). Lane l takes
+//      words l, l + 32, ... of the part and loads the matching transposed
+//      activation words once for all its rows. A packed word masked into its
+//      four field planes, (word & 0x03030303 << 2i), is multiplied by word i
+//      of the activation block with dp4a:
 //        sum_k field * x = acc0 + acc1/4 + acc2/16 + acc3/64   (each exact)
 //      and field = code + 1, so sum_k code * x = that - sum_k x.
 //   4. One shuffle reduction per row; lane 0 writes y = fp32(fp32(acc *
 //      gamma) / s) directly (P = 1) or adds into shared memory for a final
 //      pass (P > 1; integer atomics, so the order does not matter).
+// There is no shared memory and no block barrier on the P = 1 path.
 
 #include "common.cuh"
 #include "kernels.cuh"
@@ -49,25 +59,52 @@ BL_DEVICE uint32_t ld_stream_u32(const uint32_t* p) {
   return v;
 }
 
-template <int XIN> struct X8;
-template <> struct X8<kXinF32> {   // 8 fp32 values
-  static BL_DEVICE void load(const void* x, size_t off, float (&f)[8]) {
+BL_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+BL_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Coherent loads that the compiler keeps after pdl_wait(): data written by the
+// grid this kernel depends on must not come through the read-only path or be
+// hoisted above the wait.
+BL_DEVICE uint4 ld_after_wait_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+BL_DEVICE int ld_after_wait_s32(const int* p) {
+  int v;
+  asm volatile("ld.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+BL_DEVICE float ld_after_wait_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// 16 activations starting at `off`, widened exactly to fp32.
+template <int XIN>
+BL_DEVICE void load16(const void* x, size_t off, float (&f)[16]) {
+  if constexpr (XIN == kXinF32) {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + off);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-  }
-};
-template <> struct X8<kXinBF16> {  // 8 bf16 values, widened exactly
-  static BL_DEVICE void load(const void* x, size_t off, float (&f)[8]) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off));
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[2 * j] = __uint_as_float(u[j] << 16);
-      f[2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = __ldg(p + i);
+      f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 v = __ldg(p + i);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        f[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+        f[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xffff0000u);
+      }
     }
   }
-};
+}
 
 // Code of one activation, clip(rint(fp32(x * s)), -128, 127), returned in the
 // low byte (two's complement). Rounding uses the classic 1.5 * 2^23 addition:
@@ -84,29 +121,117 @@ BL_DEVICE uint32_t pack4(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
   return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
 }
 
-template <int MT> BL_DEVICE float pick(const float (&v)[MT], int m) {
-  float r = v[0];
-#pragma unroll
-  for (int i = 1; i < MT; ++i) r = (i == m) ? v[i] : r;
-  return r;
+BL_DEVICE int sum16(const uint32_t (&w)[4]) {
+  int s = dp4a_ss(static_cast<int>(w[0]), 0x01010101, 0);
+  s = dp4a_ss(static_cast<int>(w[1]), 0x01010101, s);
+  s = dp4a_ss(static_cast<int>(w[2]), 0x01010101, s);
+  return dp4a_ss(static_cast<int>(w[3]), 0x01010101, s);
+}
+
+// fp32(t / s) rounded to nearest even from r = fp32(1/s) (r = 0: use IEEE
+// division). Markstein's correction step (P. Markstein, IBM J. Res. Dev.
+// 34(1), 1990): q = RN(t * r) is within an ulp of t/s, the residual t - q*s is
+// exact in one FMA, and q + residual * r rounded once is the correctly rounded
+// quotient, barring underflow and overflow, which the range test excludes.
+BL_DEVICE float div_by_scale(float t, float s, float r) {
+  const float at = fabsf(t);
+  if (r != 0.f && (at == 0.f || (at > 0x1p-96f && at < 0x1p96f))) {
+    const float q = __fmul_rn(t, r);
+    return __fmaf_rn(__fmaf_rn(-q, s, t), r, q);
+  }
+  return __fdiv_rn(t, s);
 }
 
 }  // namespace
 
-// Shared memory (bytes, in order): activations MT * K (transposed 16-code
-// blocks); float red[kWarps][MT]; int red2[kWarps][MT]; int acc[rows][MT]
-// (only when the row is split into parts).
-//
-// KW = words per lane per part (<= kKW), RW = rows per warp (<= word_regs/kKW);
-// P divides kWarps, so warp w always works on part w % P.
-template <int MT, int KW, int XIN, bool OUT_ACC>
+// ---- 1. per-token activation pass (one CTA of kActTqThreads per token)
+template <int XIN>
+__global__ void __launch_bounds__(kActTqThreads)
+bl_act_tq(const void* __restrict__ x, const float* __restrict__ scale_in, int K, int8_t* __restrict__ xq_out,
+          float* __restrict__ scale_out, uint8_t* __restrict__ xt, int* __restrict__ rowsum) {
+  __shared__ float s_red[kActTqThreads / 32];
+  __shared__ int s_sum[kActTqThreads / 32];
+  // Wait for the previous grid (it may have produced x) before anything else,
+  // and only then let the contraction start: its early weight loads must not
+  // overtake writes of the kernels before this one.
+  pdl_wait();
+  pdl_launch_dependents();
+  const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nblk = K >> 4;
+  const size_t row = static_cast<size_t>(m) * K;
+  int part = 0;
+  if constexpr (XIN == kXinI8) {
+    for (int b = tid; b < nblk; b += blockDim.x) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const int8_t*>(x) + row) + b);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      part += sum16(w);
+      uint4 t;
+      transpose4x4_bytes(w[0], w[1], w[2], w[3], t.x, t.y, t.z, t.w);
+      *reinterpret_cast<uint4*>(xt + row + 16 * b) = t;
+    }
+    if (tid == 0 && scale_out) scale_out[m] = __ldg(scale_in + m);
+  } else {
+    float f0[16];                                   // the first block of each thread stays in registers
+    if (tid < nblk) load16<XIN>(x, row + 16 * tid, f0);
+    float amax = 0.f;
+    for (int b = tid; b < nblk; b += blockDim.x) {
+      float f[16];
+      if (b == tid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) f[j] = f0[j];
+      } else {
+        load16<XIN>(x, row + 16 * b, f);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) s_red[warp] = amax;
+    __syncthreads();
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kActTqThreads / 32; ++w) a = fmaxf(a, s_red[w]);
+    const float s = token_scale(a);
+    if (tid == 0) scale_out[m] = s;
+    for (int b = tid; b < nblk; b += blockDim.x) {
+      float f[16];
+      if (b == tid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) f[j] = f0[j];
+      } else {
+        load16<XIN>(x, row + 16 * b, f);
+      }
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = pack4(code_byte(f[4 * i], s), code_byte(f[4 * i + 1], s), code_byte(f[4 * i + 2], s),
+                     code_byte(f[4 * i + 3], s));
+      if (xq_out) *reinterpret_cast<uint4*>(xq_out + row + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
+      part += sum16(w);
+      uint4 t;
+      transpose4x4_bytes(w[0], w[1], w[2], w[3], t.x, t.y, t.z, t.w);
+      *reinterpret_cast<uint4*>(xt + row + 16 * b) = t;
+    }
+  }
+  part = warp_sum(part);
+  if (lane == 0) s_sum[warp] = part;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kActTqThreads / 32; ++w) t += s_sum[w];
+    rowsum[m] = t;
+  }
+}
+
+// ---- 2..4. the contraction (KW = words per lane per part, exact for this
+// shape; RW = rows per warp; P divides kWarps, so warp w works on part w % P)
+template <int MT, int KW, bool OUT_ACC>
 __global__ void __launch_bounds__(kGemvFusedThreads, 1)
-bl_gemv_fused(const uint8_t* __restrict__ wp, const void* __restrict__ x, const float* __restrict__ scale_in,
-              const float* __restrict__ gamma, void* __restrict__ out, int8_t* __restrict__ xq_out,
-              float* __restrict__ scale_out, int M, int N, int K, int rows_per_cta, int P) {
-  constexpr int kKW = KW;                           // words per lane per part, exact for this shape
-  constexpr int kRW = rows_per_warp(MT, kKW);
-  extern __shared__ __align__(16) uint8_t smem[];
+bl_gemv_w(const uint8_t* __restrict__ wp, const uint8_t* xt, const int* rowsum, const float* scale,
+          const float* gamma, void* __restrict__ out, int M, int N, int K, int rows_per_cta, int P) {
+  constexpr int kRW = rows_per_warp(MT, KW);
+  extern __shared__ __align__(16) int s_acc[];      // [rows][MT], only when P > 1
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n0 = blockIdx.x * rows_per_cta;
   const int R = min(rows_per_cta, N - n0);
@@ -114,16 +239,10 @@ bl_gemv_fused(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
   const int words = K >> 4;                         // packed 32-bit words per row = 16-code blocks per token
   const int part = warp % P;
   const int w_lo = part * 32 * KW;
-  const float gm = OUT_ACC ? 0.f : __ldg(gamma);
   const int row_step = kWarps / P;
 
-  uint8_t* s_x = smem;
-  float* s_red = reinterpret_cast<float*>(s_x + static_cast<size_t>(MT) * K);
-  int* s_red2 = reinterpret_cast<int*>(s_red + kWarps * MT);
-  int* s_acc = s_red2 + kWarps * MT;
-
-  // ---- 1. the warp's weight words, straight into registers
-  uint32_t wr[kRW][kKW];
+  // weight words straight into registers, before waiting for the activations
+  uint32_t wr[kRW][KW];
   const uint32_t* wbase = reinterpret_cast<const uint32_t*>(wp) + static_cast<size_t>(n0) * words + w_lo + lane;
 #pragma unroll
   for (int i = 0; i < kRW; ++i) {
@@ -131,128 +250,34 @@ bl_gemv_fused(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
     if (r < R) {                                    // warp-uniform
       const uint32_t* rp = wbase + static_cast<size_t>(r) * words;
 #pragma unroll
-      for (int j = 0; j < kKW; ++j) wr[i][j] = (w_lo + lane + 32 * j < words) ? ld_stream_u32(rp + 32 * j) : 0u;
+      for (int j = 0; j < KW; ++j) wr[i][j] = (w_lo + lane + 32 * j < words) ? ld_stream_u32(rp + 32 * j) : 0u;
     }
   }
   if (P > 1)
     for (int i = tid; i < R * MT; i += blockDim.x) s_acc[i] = 0;
+  pdl_wait();                                       // the activation pass has finished
+  pdl_launch_dependents();                          // the next grid waits for this one before its own reads
 
-  // ---- 2. activations: per-token scale, codes (transposed blocks), token sums.
-  // An item is 8 consecutive activations (half of a 16-code block); its codes
-  // land as 16-bit halves of the four transposed words of that block.
-  const int nblk = words;
-  const int nitem = 2 * nblk;                       // items per token
-  float s_tok[MT];
-  int part_sum[MT];
+  uint4 xr[KW][MT];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) part_sum[m] = 0;
-  auto stage8 = [&](int m, int it, uint32_t lo, uint32_t hi) {
-    uint8_t* blk = s_x + static_cast<size_t>(m) * K + 16 * (it >> 1) + 2 * (it & 1);
-    *reinterpret_cast<uint16_t*>(blk + 0) = static_cast<uint16_t>(__byte_perm(lo, hi, 0x0040));
-    *reinterpret_cast<uint16_t*>(blk + 4) = static_cast<uint16_t>(__byte_perm(lo, hi, 0x0051));
-    *reinterpret_cast<uint16_t*>(blk + 8) = static_cast<uint16_t>(__byte_perm(lo, hi, 0x0062));
-    *reinterpret_cast<uint16_t*>(blk + 12) = static_cast<uint16_t>(__byte_perm(lo, hi, 0x0073));
-  };
-  if constexpr (XIN == kXinI8) {
-    for (int i = tid; i < MT * nitem; i += blockDim.x) {
-      const int m = i / nitem, it = i - m * nitem;
-      uint2 v = make_uint2(0u, 0u);
-      if (m < M)
-        v = __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(x) + static_cast<size_t>(m) * K) + it);
-      const int sm = dp4a_ss(static_cast<int>(v.y), 0x01010101, dp4a_ss(static_cast<int>(v.x), 0x01010101, 0));
-#pragma unroll
-      for (int mm = 0; mm < MT; ++mm) part_sum[mm] += (mm == m) ? sm : 0;
-      stage8(m, it, v.x, v.y);
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) s_tok[m] = (OUT_ACC || m >= M) ? 1.f : __ldg(scale_in + m);
-  } else {
-    // the first item of each thread stays in registers between the passes
-    float f0[8];
-    const int m_first = tid / nitem;
-    if (tid < MT * nitem && m_first < M) X8<XIN>::load(x, static_cast<size_t>(m_first) * K + 8 * (tid - m_first * nitem), f0);
-    float amax[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) amax[m] = 0.f;
-    for (int i = tid; i < MT * nitem; i += blockDim.x) {
-      const int m = i / nitem, it = i - m * nitem;
-      if (m < M) {
-        float f[8];
-        if (i == tid) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = f0[j];
-        } else {
-          X8<XIN>::load(x, static_cast<size_t>(m) * K + 8 * it, f);
-        }
-        float a = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(f[j]));
-#pragma unroll
-        for (int mm = 0; mm < MT; ++mm) amax[mm] = (mm == m) ? fmaxf(amax[mm], a) : amax[mm];
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      const float v = warp_max(amax[m]);
-      if (lane == 0) s_red[warp * MT + m] = v;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float a = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) a = fmaxf(a, s_red[w * MT + m]);
-      s_tok[m] = token_scale(a);
-    }
-    if (scale_out && blockIdx.x == 0 && tid < M) scale_out[tid] = pick(s_tok, tid);
-    for (int i = tid; i < MT * nitem; i += blockDim.x) {
-      const int m = i / nitem, it = i - m * nitem;
-      uint32_t lo = 0u, hi = 0u;
-      if (m < M) {
-        float f[8];
-        if (i == tid) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = f0[j];
-        } else {
-          X8<XIN>::load(x, static_cast<size_t>(m) * K + 8 * it, f);
-        }
-        const float s = pick(s_tok, m);
-        lo = pack4(code_byte(f[0], s), code_byte(f[1], s), code_byte(f[2], s), code_byte(f[3], s));
-        hi = pack4(code_byte(f[4], s), code_byte(f[5], s), code_byte(f[6], s), code_byte(f[7], s));
-        if (xq_out && blockIdx.x == 0)
-          *reinterpret_cast<uint2*>(xq_out + static_cast<size_t>(m) * K + 8 * it) = make_uint2(lo, hi);
-      }
-      const int sm = dp4a_ss(static_cast<int>(hi), 0x01010101, dp4a_ss(static_cast<int>(lo), 0x01010101, 0));
-#pragma unroll
-      for (int mm = 0; mm < MT; ++mm) part_sum[mm] += (mm == m) ? sm : 0;
-      stage8(m, it, lo, hi);
-    }
-  }
-#pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    const int v = warp_sum(part_sum[m]);
-    if (lane == 0) s_red2[warp * MT + m] = v;
-  }
-  __syncthreads();   // activations staged, token sums and s_acc ready
-
-  // ---- 3. contraction from registers
-  uint4 xr[kKW][MT];
-#pragma unroll
-  for (int j = 0; j < kKW; ++j) {
+  for (int j = 0; j < KW; ++j) {
     const int wd = w_lo + lane + 32 * j;
 #pragma unroll
     for (int m = 0; m < MT; ++m)
-      xr[j][m] = (wd < words) ? *reinterpret_cast<const uint4*>(s_x + static_cast<size_t>(m) * K + 16 * wd)
-                                        : make_uint4(0u, 0u, 0u, 0u);
+      xr[j][m] = (wd < words && m < M) ? ld_after_wait_v4(xt + static_cast<size_t>(m) * K + 16 * static_cast<size_t>(wd))
+                                       : make_uint4(0u, 0u, 0u, 0u);
   }
-  int rowsum[MT];
+  int rs[MT];
+  float sc[MT], rc[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
-    int v = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) v += s_red2[w * MT + m];
-    rowsum[m] = v;
+    rs[m] = m < M ? ld_after_wait_s32(rowsum + m) : 0;
+    sc[m] = (!OUT_ACC && m < M) ? ld_after_wait_f32(scale + m) : 1.f;
+    rc[m] = (sc[m] > 0x1p-96f && sc[m] < 0x1p96f) ? __frcp_rn(sc[m]) : 0.f;
   }
+  const float gm = OUT_ACC ? 0.f : ld_after_wait_f32(gamma);
+  if (P > 1) __syncthreads();                       // s_acc cleared
+
   int vsum[kRW][MT];
 #pragma unroll
   for (int i = 0; i < kRW; ++i) {
@@ -264,7 +289,7 @@ bl_gemv_fused(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0;
 #pragma unroll
-      for (int j = 0; j < kKW; ++j) {
+      for (int j = 0; j < KW; ++j) {
         const uint32_t wv = wr[i][j];
         const uint32_t a0 = wv & 0x03030303u, a1 = wv & 0x0c0c0c0cu, a2 = wv & 0x30303030u, a3 = wv & 0xc0c0c0c0u;
 #pragma unroll
@@ -303,9 +328,10 @@ bl_gemv_fused(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
             } else {
               const size_t o = static_cast<size_t>(m) * N + n0 + r;
               if constexpr (OUT_ACC) {
-                static_cast<int32_t*>(out)[o] = vsum[i][m] - rowsum[m];
+                static_cast<int32_t*>(out)[o] = vsum[i][m] - rs[m];
               } else {
-                static_cast<float*>(out)[o] = rescale(vsum[i][m] - rowsum[m], gm, s_tok[m]);
+                static_cast<float*>(out)[o] =
+                    div_by_scale(__fmul_rn(static_cast<float>(vsum[i][m] - rs[m]), gm), sc[m], rc[m]);
               }
             }
           }
@@ -317,15 +343,22 @@ bl_gemv_fused(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
     __syncthreads();
     for (int i = tid; i < M * R; i += blockDim.x) {
       const int m = i / R, r = i - m * R;
-      int rs = 0;
+      int rsm = 0;
+      float scm = 1.f, rcm = 0.f;
 #pragma unroll
-      for (int mm = 0; mm < MT; ++mm) rs = (mm == m) ? rowsum[mm] : rs;
-      const int a = s_acc[r * MT + m] - rs;
+      for (int mm = 0; mm < MT; ++mm) {
+        if (mm == m) {
+          rsm = rs[mm];
+          scm = sc[mm];
+          rcm = rc[mm];
+        }
+      }
+      const int a = s_acc[r * MT + m] - rsm;
       const size_t o = static_cast<size_t>(m) * N + n0 + r;
       if constexpr (OUT_ACC) {
         static_cast<int32_t*>(out)[o] = a;
       } else {
-        static_cast<float*>(out)[o] = rescale(a, gm, pick(s_tok, m));
+        static_cast<float*>(out)[o] = div_by_scale(__fmul_rn(static_cast<float>(a), gm), scm, rcm);
       }
     }
   }
@@ -343,70 +376,82 @@ size_t gemv_fused_plan(int M, int N, int K, int sms, int* rows_per_cta, int* par
   int rows = (N + sms - 1) / sms;
   const int max_rows = rows_per_warp(mt, kw) * (kWarps / P);
   if (rows > max_rows) rows = max_rows;
-  const size_t smem = static_cast<size_t>(mt) * K + 2 * static_cast<size_t>(kWarps) * mt * 4 +
-                      (P > 1 ? static_cast<size_t>(rows) * mt * 4 : 0);
-  if (smem > kMaxSmemPerCta) return 0;
   *rows_per_cta = rows;
   *parts = P;
-  return smem;
+  // dynamic shared memory: the cross-part accumulators (P > 1) plus one int so
+  // the size is never zero
+  return static_cast<size_t>(P > 1 ? rows * mt * 4 : 0) + 16;
 }
 
 namespace {
 
-template <int MT, int KW, int XIN, bool OUT_ACC>
-cudaError_t launch_t(const uint8_t* wp, const void* x, const float* scale_in, const float* gamma, void* out,
-                     int8_t* xq_out, float* scale_out, int M, int N, int K, int rows, int P, size_t smem,
-                     cudaStream_t s) {
-  static size_t done = 48 * 1024;   // shared-memory attribute, raised once per instance and size
-  if (smem > done) {
-    cudaError_t e = cudaFuncSetAttribute(bl_gemv_fused<MT, KW, XIN, OUT_ACC>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    done = smem;
-  }
+template <typename... Args>
+cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int MT, int KW, bool OUT_ACC>
+cudaError_t launch_w(const uint8_t* wp, const uint8_t* xt, const int* rowsum, const float* scale, const float* gamma,
+                     void* out, int M, int N, int K, int rows, int P, size_t smem, cudaStream_t s) {
   const int grid = (N + rows - 1) / rows;
-  bl_gemv_fused<MT, KW, XIN, OUT_ACC><<<grid, kGemvFusedThreads, smem, s>>>(wp, x, scale_in, gamma, out, xq_out,
-                                                                            scale_out, M, N, K, rows, P);
-  return cudaGetLastError();
+  return launch_dependent(bl_gemv_w<MT, KW, OUT_ACC>, dim3(grid), dim3(kGemvFusedThreads), smem, s, wp, xt, rowsum,
+                          scale, gamma, out, M, N, K, rows, P);
 }
 
 template <int MT, int KW>
-cudaError_t pick_io(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma, void* out,
-                    bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K, int rows, int P, size_t smem,
-                    cudaStream_t s) {
-  // fp32 / bf16 activations always produce y; the int32 accumulator comes from int8 input
-  if (xin == kXinF32) return launch_t<MT, KW, kXinF32, false>(wp, x, scale_in, gamma, out, xq_out, scale_out, M, N, K, rows, P, smem, s);
-  if (xin == kXinBF16) return launch_t<MT, KW, kXinBF16, false>(wp, x, scale_in, gamma, out, xq_out, scale_out, M, N, K, rows, P, smem, s);
-  if (out_acc) return launch_t<MT, KW, kXinI8, true>(wp, x, scale_in, gamma, out, xq_out, scale_out, M, N, K, rows, P, smem, s);
-  return launch_t<MT, KW, kXinI8, false>(wp, x, scale_in, gamma, out, xq_out, scale_out, M, N, K, rows, P, smem, s);
-}
-
-template <int MT, int KW>
-cudaError_t pick_kw(int kw, const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
-                    void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K, int rows, int P,
+cudaError_t pick_kw(int kw, bool out_acc, const uint8_t* wp, const uint8_t* xt, const int* rowsum,
+                    const float* scale, const float* gamma, void* out, int M, int N, int K, int rows, int P,
                     size_t smem, cudaStream_t s) {
   if constexpr (KW > 1) {
     if (kw < KW)
-      return pick_kw<MT, KW - 1>(kw, wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out, M, N, K, rows, P, smem, s);
+      return pick_kw<MT, KW - 1>(kw, out_acc, wp, xt, rowsum, scale, gamma, out, M, N, K, rows, P, smem, s);
   }
-  return pick_io<MT, KW>(wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out, M, N, K, rows, P, smem, s);
+  if (out_acc) return launch_w<MT, KW, true>(wp, xt, rowsum, scale, gamma, out, M, N, K, rows, P, smem, s);
+  return launch_w<MT, KW, false>(wp, xt, rowsum, scale, gamma, out, M, N, K, rows, P, smem, s);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
                               void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K,
-                              int rows_per_cta, int parts, size_t smem, cudaStream_t s) {
-  if ((xin == kXinF32 || xin == kXinBF16) && out_acc) return cudaErrorInvalidValue;
+                              int rows_per_cta, int parts, size_t smem, void* workspace, cudaStream_t s) {
+  uint8_t* xt = static_cast<uint8_t*>(workspace);
+  uint8_t* b = xt + ((static_cast<size_t>(M) * K + 255) & ~size_t(255));
+  int* rowsum = reinterpret_cast<int*>(b);
+  float* sc = reinterpret_cast<float*>(b + ((static_cast<size_t>(M) * 4 + 255) & ~size_t(255)));
+  if (scale_out) sc = scale_out;
+  cudaError_t e;
+  if (xin == kXinF32)
+    e = launch_dependent(bl_act_tq<kXinF32>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K, xq_out, sc, xt,
+                         rowsum);
+  else if (xin == kXinBF16)
+    e = launch_dependent(bl_act_tq<kXinBF16>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K, xq_out, sc, xt,
+                         rowsum);
+  else
+    e = launch_dependent(bl_act_tq<kXinI8>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K,
+                         static_cast<int8_t*>(nullptr), static_cast<float*>(nullptr), xt, rowsum);
+  if (e != cudaSuccess) return e;
+  const float* scale = (xin == kXinI8) ? scale_in : sc;
   const int words = K / 16;
   const int kw = (words + 32 * parts - 1) / (32 * parts);
-  if (M <= 1) return pick_kw<1, 8>(kw, wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out, M, N, K, rows_per_cta, parts, smem, s);
-  if (M <= 2) return pick_kw<2, 4>(kw, wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out, M, N, K, rows_per_cta, parts, smem, s);
-  return pick_kw<4, 2>(kw, wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out, M, N, K, rows_per_cta, parts, smem, s);
+  if (M <= 1) return pick_kw<1, 8>(kw, out_acc, wp, xt, rowsum, scale, gamma, out, M, N, K, rows_per_cta, parts, smem, s);
+  if (M <= 2) return pick_kw<2, 4>(kw, out_acc, wp, xt, rowsum, scale, gamma, out, M, N, K, rows_per_cta, parts, smem, s);
+  return pick_kw<4, 2>(kw, out_acc, wp, xt, rowsum, scale, gamma, out, M, N, K, rows_per_cta, parts, smem, s);
 }
 
 cudaError_t take_gemv_wait_error(int* flag) {
-  *flag = 0;   // this kernel has no asynchronous copies to wait for
+  *flag = 0;   // this path has no asynchronous copies to wait for
   return cudaSuccess;
 }
 

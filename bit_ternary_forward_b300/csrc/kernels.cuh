@@ -58,16 +58,21 @@ cudaError_t launch_decode(const uint8_t* wp, const void* x, int xin, const float
 // Reads and clears the device word set when a bounded wait gave up (synchronous).
 cudaError_t take_wait_error(int* flag);
 
-// ---- decode GEMV for M <= 4 with fused activation quantisation (gemv_fused.cu)
+// ---- decode GEMV for M <= 4: per-token activation pass + contraction (gemv_fused.cu)
 constexpr int kGemvFusedThreads = 512;
+constexpr int kActTqThreads = 256;
 constexpr int kGemvFusedMaxM = 4;
 // Chooses rows per CTA and the number of k-parts for M x N x K on `sms` SMs;
-// returns the dynamic shared memory in bytes, or 0 if the kernel does not take
-// the shape (M > 4, K % 64 != 0, K too long).
+// returns the contraction's dynamic shared memory in bytes (never 0), or 0 if
+// the path does not take the shape (M > 4, K % 64 != 0, K too long).
 size_t gemv_fused_plan(int M, int N, int K, int sms, int* rows_per_cta, int* parts);
+// Launches both kernels. workspace: the transposed codes (M*K bytes, rounded up
+// to 256), then int token sums [M] (rounded up to 256), then fp32 scales [M]
+// (used when scale_out is NULL). With xin == kXinI8, x is x_q and scale_in its
+// scales; out is fp32 y or int32 acc (out_acc).
 cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
                               void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K,
-                              int rows_per_cta, int parts, size_t smem, cudaStream_t s);
+                              int rows_per_cta, int parts, size_t smem, void* workspace, cudaStream_t s);
 cudaError_t take_gemv_wait_error(int* flag);
 
 // ---- prefill contraction on tcgen05 (prefill.cu)

@@ -194,18 +194,30 @@ bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_
     if (lane == 0) s_part[warp][l] = v;
   }
   __syncthreads();
+  // limb l summed over the warps by thread l: 32-bit halves kept apart so no
+  // 64-bit sum can wrap (each warp value is below 2^32 * n_partials)
+  __shared__ unsigned long long s_lo[kLimbs], s_hi[kLimbs];
+  if (tid < kLimbs) {
+    unsigned long long lo = 0, hi = 0;
+#pragma unroll
+    for (int w = 0; w < 256 / 32; ++w) {
+      lo += s_part[w][tid] & 0xffffffffull;
+      hi += s_part[w][tid] >> 32;
+    }
+    s_lo[tid] = lo;
+    s_hi[tid] = hi;
+  }
+  __syncthreads();
   if (tid != 0) return;
 
   // exact sum S in 32-bit limbs (S < 2^309)
   uint32_t S[kLimbs + 1];
   unsigned long long carry = 0;
+#pragma unroll
   for (int l = 0; l < kLimbs; ++l) {
-    unsigned long long v = carry;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) v += s_part[w][l] & 0xffffffffull;
-    unsigned long long hi = 0;
-    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) hi += s_part[w][l] >> 32;
+    const unsigned long long v = carry + s_lo[l];
     S[l] = static_cast<uint32_t>(v);
-    carry = (v >> 32) + hi;
+    carry = (v >> 32) + s_hi[l];
   }
   S[kLimbs] = static_cast<uint32_t>(carry);
 
