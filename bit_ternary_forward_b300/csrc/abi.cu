@@ -225,14 +225,27 @@ bl_status check_pack_args(const float* W, int64_t N, int64_t K, const void* Wp_o
   return BL_OK;
 }
 
+// CTAs of the exact-sum kernel that are resident on one SM at a time.
+int absum_ctas_per_sm() {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bl::bl_absum_partials, bl::kAbsumThreads, 0) != cudaSuccess ||
+        n <= 0)
+      n = 4;
+    per_sm = n;
+  }
+  return per_sm;
+}
+
 bl_status run_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* workspace, cudaStream_t s) {
   const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
   const uint64_t n4 = nk / 4;
   const int sms = sm_count();
   uint64_t ga = (n4 + bl::kAbsumThreads * 4 - 1) / (bl::kAbsumThreads * 4);
-  const uint64_t cap = static_cast<uint64_t>(sms) * 8 < static_cast<uint64_t>(bl::kMaxAbsumCtas)
-                           ? static_cast<uint64_t>(sms) * 8
-                           : static_cast<uint64_t>(bl::kMaxAbsumCtas);
+  // one full wave: a second, partial wave of CTAs would trail the first
+  const uint64_t wave = static_cast<uint64_t>(sms) * static_cast<uint64_t>(absum_ctas_per_sm());
+  const uint64_t cap = wave < static_cast<uint64_t>(bl::kMaxAbsumCtas) ? wave : static_cast<uint64_t>(bl::kMaxAbsumCtas);
   if (ga > cap) ga = cap;
   if (ga < 1) ga = 1;
   uint32_t* partials = static_cast<uint32_t*>(workspace);
@@ -248,8 +261,14 @@ bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, const float* g
   const uint64_t n_bytes = nk / 4;
   const uint64_t n_words = n_bytes / 4;
   const int sms = sm_count();
+  static int per_sm = 0;   // resident CTAs of bl_quant_pack per SM: one full wave
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bl::bl_quant_pack, 256, 0) != cudaSuccess || n <= 0) n = 4;
+    per_sm = n;
+  }
   uint64_t gq = (n_words + 255) / 256;
-  if (gq > static_cast<uint64_t>(sms) * 8) gq = static_cast<uint64_t>(sms) * 8;
+  if (gq > static_cast<uint64_t>(sms) * per_sm) gq = static_cast<uint64_t>(sms) * per_sm;
   if (gq < 1) gq = 1;
   bl::bl_quant_pack<<<static_cast<unsigned>(gq), 256, 0, s>>>(reinterpret_cast<const float4*>(W), n_bytes, gamma,
                                                                reinterpret_cast<uint32_t*>(Wp));

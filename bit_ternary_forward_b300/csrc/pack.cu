@@ -15,12 +15,16 @@
 //
 //   1. bl_absum_partials: each CTA sums its share of |W| exactly. Each warp
 //      picks a window of 32 binades from the largest exponent among its first
-//      128 weights (4 binades above it, 27 below); a lane adds every weight
-//      inside the window, as its 24-bit significand shifted into place, to a
-//      96-bit register accumulator (add with carry); weights outside the
-//      window (zeros, subnormals, stragglers far from the warp's scale) go to
-//      254 per-exponent 64-bit bins in shared memory. The CTA folds both into
-//      a 384-bit fixed-point partial (12 x 32-bit limbs).
+//      128 weights (4 binades above it, 27 below). For a weight in the window,
+//      at distance d binades above its bottom, |w| = m * 2^d window units (m
+//      the 24-bit significand), which one wide multiply-add (mad.wide.u32)
+//      adds to a 64-bit register accumulator; 2^d comes from a shift that
+//      gives 0 for any d outside 0..31, so out-of-window weights add nothing
+//      there. One OR over the four shift amounts of a float4 finds those
+//      weights (zeros, subnormals, stragglers far from the warp's scale);
+//      they go to 254 per-exponent 64-bit bins in shared memory. The 64-bit
+//      accumulator is folded into 96 bits after every 16 weights, and the CTA
+//      folds everything into a 384-bit fixed-point partial (12 x 32-bit limbs).
 //   2. bl_gamma_finalize: one CTA adds the partials (shuffle reductions), then
 //      one thread divides the top 64 bits of the exact sum by N*K and rounds
 //      the quotient to fp32, ties to even, with the dropped bits and the
@@ -40,7 +44,8 @@ constexpr int kLimbs = 12;            // 384-bit fixed point, units of 2^-149
 constexpr int kSmemLimbs = 16;        // headroom for shifted pieces
 constexpr int kBins = 256;
 
-BL_DEVICE float4 ld_stream_f4(const float4* p) {
+// Streaming 16-byte load that does not allocate in L1.
+BL_DEVICE float4 ld_f4_stream(const float4* p) {
   float4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
@@ -80,6 +85,20 @@ BL_DEVICE void add_words_shifted(unsigned long long* limbs, const uint32_t (&w)[
 
 BL_DEVICE int exp_field(float x) { return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu); }
 
+// a << s with PTX semantics: shift amounts of 32 or more give 0.
+BL_DEVICE uint32_t shl_clamped(uint32_t a, uint32_t s) {
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(s));
+  return r;
+}
+
+// a * b + c with a 64-bit addend and result (exact while it stays below 2^64).
+BL_DEVICE unsigned long long mad_wide_u32(uint32_t a, uint32_t b, unsigned long long c) {
+  unsigned long long r;
+  asm("mad.wide.u32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(c));
+  return r;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kAbsumThreads)
@@ -93,10 +112,11 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
 
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   const uint64_t first = static_cast<uint64_t>(blockIdx.x) * blockDim.x + tid;
+  auto ld_stream_f4 = [](const float4* p) { return ld_f4_stream(p); };
 
   // Warp-uniform window [base, base + 31] in units of 2^-149; a normal weight
   // with exponent field e and significand m (implicit bit included) is
-  // m * 2^(e - 1) in those units.
+  // m * 2^(e - 1) in those units, so d = e - 1 - base.
   float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (first < n4) v0 = ld_stream_f4(w4 + first);
   int e_loc = max(max(exp_field(v0.x), exp_field(v0.y)), max(exp_field(v0.z), exp_field(v0.w)));
@@ -107,35 +127,65 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
   const uint32_t bias = static_cast<uint32_t>(base) + 1u;
   __syncthreads();   // bins and limbs cleared
 
-  uint32_t a0 = 0u, a1 = 0u, a2 = 0u;
-  auto take = [&](float x) {
-    const uint32_t b = __float_as_uint(x);
-    const uint32_t e = (b >> 23) & 0xffu;
-    const uint32_t d = e - bias;                      // wraps for e == 0 and below the window
-    if (d < 32u) {
-      const uint32_t m = (b & 0x7fffffu) | 0x800000u;
-      add96(a0, a1, a2, m << d, __funnelshift_l(m, 0u, d));
-    } else if (b & 0x7fffffffu) {
-      const uint32_t m = e ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
+  uint32_t a0 = 0u, a1 = 0u, a2 = 0u;      // 96-bit total
+  unsigned long long acc = 0ull;           // at most 16 window terms below 2^55 each
+
+  // out-of-window weights of a float4 (rare): exact per-exponent bins
+  auto rare = [&](float x) {
+    const uint32_t b = __float_as_uint(x) & 0x7fffffffu;
+    const uint32_t e = b >> 23;
+    if ((e - bias) >= 32u && b != 0u) {
+      const uint32_t m = e ? ((b & 0x7fffffu) | 0x800000u) : b;
       atomicAdd(&s_bins[e ? e - 1u : 0u], static_cast<unsigned long long>(m));
     }
   };
+  auto take4 = [&](const float4& v) {
+    const uint32_t b0 = __float_as_uint(v.x) & 0x7fffffffu, b1 = __float_as_uint(v.y) & 0x7fffffffu;
+    const uint32_t b2 = __float_as_uint(v.z) & 0x7fffffffu, b3 = __float_as_uint(v.w) & 0x7fffffffu;
+    const uint32_t d0 = (b0 >> 23) - bias, d1 = (b1 >> 23) - bias, d2 = (b2 >> 23) - bias, d3 = (b3 >> 23) - bias;
+    acc = mad_wide_u32((b0 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d0), acc);
+    acc = mad_wide_u32((b1 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d1), acc);
+    acc = mad_wide_u32((b2 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d2), acc);
+    acc = mad_wide_u32((b3 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d3), acc);
+    if ((d0 | d1 | d2 | d3) >= 32u) {
+      rare(v.x); rare(v.y); rare(v.z); rare(v.w);
+    }
+  };
+  auto fold = [&]() {
+    add96(a0, a1, a2, static_cast<uint32_t>(acc), static_cast<uint32_t>(acc >> 32));
+    acc = 0ull;
+  };
 
   if (first < n4) {
-    take(v0.x); take(v0.y); take(v0.z); take(v0.w);
+    take4(v0);
+    fold();
   }
+  // software pipeline: the next four float4 of this thread are in flight while
+  // the current four are summed
   uint64_t i = first + stride;
-  for (; i + 3 * stride < n4; i += 4 * stride) {
-    const float4 u0 = ld_stream_f4(w4 + i), u1 = ld_stream_f4(w4 + i + stride);
-    const float4 u2 = ld_stream_f4(w4 + i + 2 * stride), u3 = ld_stream_f4(w4 + i + 3 * stride);
-    take(u0.x); take(u0.y); take(u0.z); take(u0.w);
-    take(u1.x); take(u1.y); take(u1.z); take(u1.w);
-    take(u2.x); take(u2.y); take(u2.z); take(u2.w);
-    take(u3.x); take(u3.y); take(u3.z); take(u3.w);
+  float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
+  bool have = i + 3 * stride < n4;
+  if (have) {
+    c0 = ld_stream_f4(w4 + i); c1 = ld_stream_f4(w4 + i + stride);
+    c2 = ld_stream_f4(w4 + i + 2 * stride); c3 = ld_stream_f4(w4 + i + 3 * stride);
+  }
+  while (have) {
+    const uint64_t nxt = i + 4 * stride;
+    const bool more = nxt + 3 * stride < n4;
+    float4 p0 = c0, p1 = c1, p2 = c2, p3 = c3;
+    if (more) {
+      p0 = ld_stream_f4(w4 + nxt); p1 = ld_stream_f4(w4 + nxt + stride);
+      p2 = ld_stream_f4(w4 + nxt + 2 * stride); p3 = ld_stream_f4(w4 + nxt + 3 * stride);
+    }
+    take4(c0); take4(c1); take4(c2); take4(c3);
+    fold();
+    c0 = p0; c1 = p1; c2 = p2; c3 = p3;
+    i = nxt;
+    have = more;
   }
   for (; i < n4; i += stride) {
-    const float4 u = ld_stream_f4(w4 + i);
-    take(u.x); take(u.y); take(u.z); take(u.w);
+    take4(ld_stream_f4(w4 + i));
+    fold();
   }
 
   // warp sum of the 96-bit accumulators (all lanes share `base`)
@@ -279,14 +329,30 @@ BL_DEVICE uint32_t pack16(const float4& a, const float4& b, const float4& c, con
 __global__ void __launch_bounds__(256)
 bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __restrict__ gamma,
               uint32_t* __restrict__ wp_words) {
-  const float d = __fadd_rn(*gamma, kEpsGamma);
-  const float h = 0.5f * d;                 // exact: d is a normal fp32
   const uint64_t n_words = n_bytes >> 2;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_words; i += stride) {
+  uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // software pipeline: the next word's 16 weights load while this one packs,
+  // and the first loads are in flight before gamma arrives
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c = a, e = a;
+  if (i < n_words) {
     const float4* src = w4 + 4 * i;
-    float4 a = __ldcs(src), b = __ldcs(src + 1), c = __ldcs(src + 2), e = __ldcs(src + 3);
+    a = ld_f4_stream(src); b = ld_f4_stream(src + 1);
+    c = ld_f4_stream(src + 2); e = ld_f4_stream(src + 3);
+  }
+  const float d = __fadd_rn(*gamma, kEpsGamma);
+  const float h = 0.5f * d;                 // exact: d is a normal fp32
+  while (i < n_words) {
+    const uint64_t nxt = i + stride;
+    float4 na = a, nb = b, nc = c, ne = e;
+    if (nxt < n_words) {
+      const float4* src = w4 + 4 * nxt;
+      na = ld_f4_stream(src); nb = ld_f4_stream(src + 1);
+      nc = ld_f4_stream(src + 2); ne = ld_f4_stream(src + 3);
+    }
     wp_words[i] = pack16(a, b, c, e, h);
+    a = na; b = nb; c = nc; e = ne;
+    i = nxt;
   }
   // tail: up to three bytes when N*K/4 is not a multiple of 4
   const uint64_t t = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
