@@ -24,12 +24,6 @@ bl_status fail(bl_status st, const char* fmt, ...) {
   return st;
 }
 
-bl_status check_launch(const char* what) {
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
-  return BL_OK;
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -249,11 +243,13 @@ bl_status run_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* 
   if (ga > cap) ga = cap;
   if (ga < 1) ga = 1;
   uint32_t* partials = static_cast<uint32_t*>(workspace);
-  bl::bl_absum_partials<<<static_cast<unsigned>(ga), bl::kAbsumThreads, 0, s>>>(
-      reinterpret_cast<const float4*>(W), n4, partials);
-  if (bl_status st = check_launch("bl_absum_partials")) return st;
-  bl::bl_gamma_finalize<<<1, 256, 0, s>>>(partials, static_cast<int>(ga), nk, gamma);
-  return check_launch("bl_gamma_finalize");
+  cudaError_t e = bl::launch_pdl(bl::bl_absum_partials, dim3(static_cast<unsigned>(ga)), dim3(bl::kAbsumThreads), 0, s,
+                                 reinterpret_cast<const float4*>(W), n4, partials);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_absum_partials: %s", cudaGetErrorString(e));
+  e = bl::launch_pdl(bl::bl_gamma_finalize, dim3(1), dim3(256), 0, s, static_cast<const uint32_t*>(partials),
+                     static_cast<int>(ga), nk, gamma);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gamma_finalize: %s", cudaGetErrorString(e));
+  return BL_OK;
 }
 
 bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma, uint8_t* Wp, cudaStream_t s) {
@@ -270,9 +266,10 @@ bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, const float* g
   uint64_t gq = (n_words + 255) / 256;
   if (gq > static_cast<uint64_t>(sms) * per_sm) gq = static_cast<uint64_t>(sms) * per_sm;
   if (gq < 1) gq = 1;
-  bl::bl_quant_pack<<<static_cast<unsigned>(gq), 256, 0, s>>>(reinterpret_cast<const float4*>(W), n_bytes, gamma,
-                                                               reinterpret_cast<uint32_t*>(Wp));
-  return check_launch("bl_quant_pack");
+  cudaError_t e = bl::launch_pdl(bl::bl_quant_pack, dim3(static_cast<unsigned>(gq)), dim3(256), 0, s,
+                                 reinterpret_cast<const float4*>(W), n_bytes, gamma, reinterpret_cast<uint32_t*>(Wp));
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_quant_pack: %s", cudaGetErrorString(e));
+  return BL_OK;
 }
 
 bl_status check_pack_workspace(int64_t N, int64_t K, const void* workspace, size_t ws_bytes) {

@@ -37,6 +37,9 @@ __global__ void __launch_bounds__(kActThreads)
 bl_act_quant(const T* __restrict__ x, int K, int8_t* __restrict__ xq, float* __restrict__ scale) {
   using V = typename Vec4<T>::type;
   __shared__ float s_red[kActThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  x = launder(x);
   const int m = blockIdx.x;
   const V* row = reinterpret_cast<const V*>(x + static_cast<size_t>(m) * K);
   const int nv = K >> 2;   // K % 4 == 0
@@ -72,12 +75,9 @@ bl_act_quant(const T* __restrict__ x, int K, int8_t* __restrict__ xq, float* __r
 }
 
 cudaError_t launch_act_quant(const void* x, bool bf16, int M, int K, int8_t* xq, float* scale, cudaStream_t s) {
-  if (bf16) {
-    bl_act_quant<uint16_t><<<M, kActThreads, 0, s>>>(static_cast<const uint16_t*>(x), K, xq, scale);
-  } else {
-    bl_act_quant<float><<<M, kActThreads, 0, s>>>(static_cast<const float*>(x), K, xq, scale);
-  }
-  return cudaGetLastError();
+  if (bf16) return launch_pdl(bl_act_quant<uint16_t>, dim3(M), dim3(kActThreads), 0, s,
+                              static_cast<const uint16_t*>(x), K, xq, scale);
+  return launch_pdl(bl_act_quant<float>, dim3(M), dim3(kActThreads), 0, s, static_cast<const float*>(x), K, xq, scale);
 }
 
 }  // namespace bl

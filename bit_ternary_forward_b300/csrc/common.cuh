@@ -79,4 +79,23 @@ BL_DEVICE float rescale(int acc, float gamma, float s) {
   return __fdiv_rn(__fmul_rn(static_cast<float>(acc), gamma), s);
 }
 
+// Programmatic dependent launch. Every kernel of this library runs
+//   prologue (no global reads) -> pdl_wait() -> pdl_launch_dependents() -> body
+// so a grid may become resident before its predecessor ends, no read of the
+// body can see a partial write of the predecessor (pdl_wait returns once the
+// predecessor has completed and its memory is visible), and the dependent
+// grid, released only after this grid's own wait, cannot overtake writes of
+// anything earlier. Both are no-ops for a grid launched without the attribute.
+BL_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+BL_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The same pointer, opaque to the compiler: loads through it cannot be hoisted
+// above the asm (read-only loads could otherwise move above pdl_wait()).
+template <typename T>
+BL_DEVICE T* launder(T* p) {
+  T* q;
+  asm volatile("mov.b64 %0, %1;" : "=l"(q) : "l"(p) : "memory");
+  return q;
+}
+
 }  // namespace bl

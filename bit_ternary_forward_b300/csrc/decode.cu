@@ -169,6 +169,11 @@ bl_decode_mma(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
   float* s_red = s_scale + kTok;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(s_red + kWarps * kTok) + 7) & ~uintptr_t(7));
 
+  pdl_wait();
+  pdl_launch_dependents();
+  x = launder(x);
+  scale_in = launder(scale_in);
+  gamma = launder(gamma);
   // ---- issue the weight copies (one thread), one mbarrier per 16-row tile
   if (tid == 0) {
     for (int tl = 0; tl < n_tiles; ++tl) mbar_init(&s_bar[tl], 1);
@@ -386,9 +391,8 @@ cudaError_t launch_decode_t(const uint8_t* wp, const void* x, const float* scale
   cudaError_t e = set_smem<XIN, OUT_ACC>(smem);
   if (e != cudaSuccess) return e;
   const int grid = (N + rows_per_cta - 1) / rows_per_cta;
-  bl_decode_mma<XIN, OUT_ACC><<<grid, kDecodeThreads, smem, s>>>(wp, x, scale_in, gamma, out, xq_out, scale_out, M, N,
-                                                                  K, rows_per_cta);
-  return cudaGetLastError();
+  return launch_pdl(bl_decode_mma<XIN, OUT_ACC>, dim3(grid), dim3(kDecodeThreads), smem, s, wp, x, scale_in, gamma,
+                    out, xq_out, scale_out, M, N, K, rows_per_cta);
 }
 
 cudaError_t launch_decode(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,

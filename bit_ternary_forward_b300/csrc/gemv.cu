@@ -46,6 +46,12 @@ bl_gemv_w2a8(const uint8_t* __restrict__ wp, const int8_t* __restrict__ xq,
              void* __restrict__ out, int M, int N, int K) {
   extern __shared__ __align__(16) uint8_t s_x[];          // MT x Kp transposed activations
   __shared__ int s_rowsum[MT];
+  pdl_wait();
+  pdl_launch_dependents();
+  wp = launder(wp);
+  xq = launder(xq);
+  scale = launder(scale);
+  gamma = launder(gamma);
   const int Kp = (K + 63) & ~63;                          // staging row length, zero padded
   const int m0 = blockIdx.y * MT;
   const int mcount = min(MT, M - m0);
@@ -169,8 +175,7 @@ cudaError_t launch_gemv(const uint8_t* wp, const int8_t* xq, const float* scale,
     if (e != cudaSuccess) return e;
   }
   dim3 grid(grid_x, (M + mt - 1) / mt);
-  fn<<<grid, kGemvThreads, smem, s>>>(wp, xq, scale, gamma, out, M, N, K);
-  return cudaGetLastError();
+  return launch_pdl(fn, grid, dim3(kGemvThreads), smem, s, wp, xq, scale, gamma, out, M, N, K);
 }
 
 }  // namespace bl

@@ -59,9 +59,6 @@ BL_DEVICE uint32_t ld_stream_u32(const uint32_t* p) {
   return v;
 }
 
-BL_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-BL_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Coherent loads that the compiler keeps after pdl_wait(): data written by the
 // grid this kernel depends on must not come through the read-only path or be
 // hoisted above the wait.
@@ -385,27 +382,11 @@ size_t gemv_fused_plan(int M, int N, int K, int sms, int* rows_per_cta, int* par
 
 namespace {
 
-template <typename... Args>
-cudaError_t launch_dependent(void (*kern)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                             Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 template <int MT, int KW, bool OUT_ACC>
 cudaError_t launch_w(const uint8_t* wp, const uint8_t* xt, const int* rowsum, const float* scale, const float* gamma,
                      void* out, int M, int N, int K, int rows, int P, size_t smem, cudaStream_t s) {
   const int grid = (N + rows - 1) / rows;
-  return launch_dependent(bl_gemv_w<MT, KW, OUT_ACC>, dim3(grid), dim3(kGemvFusedThreads), smem, s, wp, xt, rowsum,
+  return launch_pdl(bl_gemv_w<MT, KW, OUT_ACC>, dim3(grid), dim3(kGemvFusedThreads), smem, s, wp, xt, rowsum,
                           scale, gamma, out, M, N, K, rows, P);
 }
 
@@ -433,13 +414,13 @@ cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const f
   if (scale_out) sc = scale_out;
   cudaError_t e;
   if (xin == kXinF32)
-    e = launch_dependent(bl_act_tq<kXinF32>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K, xq_out, sc, xt,
+    e = launch_pdl(bl_act_tq<kXinF32>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K, xq_out, sc, xt,
                          rowsum);
   else if (xin == kXinBF16)
-    e = launch_dependent(bl_act_tq<kXinBF16>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K, xq_out, sc, xt,
+    e = launch_pdl(bl_act_tq<kXinBF16>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K, xq_out, sc, xt,
                          rowsum);
   else
-    e = launch_dependent(bl_act_tq<kXinI8>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K,
+    e = launch_pdl(bl_act_tq<kXinI8>, dim3(M), dim3(kActTqThreads), 0, s, x, scale_in, K,
                          static_cast<int8_t*>(nullptr), static_cast<float*>(nullptr), xt, rowsum);
   if (e != cudaSuccess) return e;
   const float* scale = (xin == kXinI8) ? scale_in : sc;

@@ -113,6 +113,9 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   const uint64_t first = static_cast<uint64_t>(blockIdx.x) * blockDim.x + tid;
   auto ld_stream_f4 = [](const float4* p) { return ld_f4_stream(p); };
+  pdl_wait();
+  pdl_launch_dependents();
+  w4 = launder(w4);
 
   // Warp-uniform window [base, base + 31] in units of 2^-149; a normal weight
   // with exponent field e and significand m (implicit bit included) is
@@ -226,6 +229,9 @@ bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_
                   float* __restrict__ gamma) {
   __shared__ unsigned long long s_part[256 / 32][kLimbs];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+  partials = launder(partials);
   unsigned long long loc[kLimbs];
 #pragma unroll
   for (int l = 0; l < kLimbs; ++l) loc[l] = 0ull;
@@ -332,6 +338,10 @@ bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __re
   const uint64_t n_words = n_bytes >> 2;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
   uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  w4 = launder(w4);
+  gamma = launder(gamma);
   // software pipeline: the next word's 16 weights load while this one packs,
   // and the first loads are in flight before gamma arrives
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c = a, e = a;

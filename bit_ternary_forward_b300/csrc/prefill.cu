@@ -249,6 +249,11 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();                                    // inputs come from the grid before (TMA reads after this)
+  pdl_launch_dependents();
+  scale = launder(scale);
+  rowsum = launder(rowsum);
+  gamma = launder(gamma);
 
   if (warp == 0) {
     // ---- TMA producer
@@ -498,6 +503,10 @@ __global__ void __launch_bounds__(256)
 bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int M, int K,
             int8_t* __restrict__ xq_out, float* __restrict__ scale_out, __half* __restrict__ xperm,
             int* __restrict__ rowsum) {
+  pdl_wait();
+  pdl_launch_dependents();
+  x = launder(x);
+  scale_in = launder(scale_in);
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (m >= M) return;
@@ -629,8 +638,8 @@ cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
   }
   const int tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   const int grid = tiles < sms ? tiles : sms;
-  bl_gemm_tc<BN, OUT_ACC><<<grid, kThreads, smem, s>>>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K);
-  return cudaGetLastError();
+  return launch_pdl(bl_gemm_tc<BN, OUT_ACC>, dim3(grid), dim3(kThreads), smem, s, tm_x, tm_w, scale, rowsum, gamma,
+                    out, M, N, K);
 }
 
 template <bool OUT_ACC>
@@ -653,12 +662,12 @@ cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M
   __half* xp = static_cast<__half*>(xperm);
   const int grid = (M + 7) / 8;
   if (xin == kXinF32)
-    bl_act_perm<kXinF32><<<grid, 256, 0, s>>>(x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
-  else if (xin == kXinBF16)
-    bl_act_perm<kXinBF16><<<grid, 256, 0, s>>>(x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
-  else
-    bl_act_perm<kXinI8><<<grid, 256, 0, s>>>(x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
-  return cudaGetLastError();
+    return launch_pdl(bl_act_perm<kXinF32>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
+                      rowsum);
+  if (xin == kXinBF16)
+    return launch_pdl(bl_act_perm<kXinBF16>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
+                      rowsum);
+  return launch_pdl(bl_act_perm<kXinI8>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
 }
 
 cudaError_t launch_gemm_tc(const void* xperm, const uint8_t* wp, const float* scale, const int* rowsum,
