@@ -193,12 +193,13 @@ int bitlinear_version(void) { return 1; }
 bl_status bitlinear_device_error(int* flag) {
   g_last_error.clear();
   if (!flag) return fail(BL_ERR_INVALID_ARG, "null pointer (flag)");
-  int a = 0, b = 0, c = 0;
+  int a = 0, b = 0, c = 0, d = 0;
   cudaError_t e = bl::take_wait_error(&a);
   if (e == cudaSuccess) e = bl::take_gemv_wait_error(&b);
   if (e == cudaSuccess) e = bl::take_tc_wait_error(&c);
+  if (e == cudaSuccess) e = bl::take_pack_wait_error(&d);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bitlinear_device_error: %s", cudaGetErrorString(e));
-  *flag = a | b | c;
+  *flag = a | b | c | d;
   return BL_OK;
 }
 
@@ -219,55 +220,55 @@ bl_status check_pack_args(const float* W, int64_t N, int64_t K, const void* Wp_o
   return BL_OK;
 }
 
-// CTAs of the exact-sum kernel that are resident on one SM at a time.
-int absum_ctas_per_sm() {
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bl::bl_absum_partials, bl::kAbsumThreads, 0) != cudaSuccess ||
-        n <= 0)
-      n = 4;
-    per_sm = n;
-  }
-  return per_sm;
+// Resident CTAs per SM of a ring kernel with kRingSmem bytes of dynamic shared
+// memory and `threads` threads (0 when the shared memory cannot be reserved).
+int ring_ctas_per_sm(const void* kern, int threads) {
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bl::kRingSmem)) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, bl::kRingSmem) != cudaSuccess)
+    n = 0;
+  return n;
+}
+
+// One wave of ring CTAs, each with at least one stage of work.
+uint64_t ring_grid(uint64_t stages, int per_sm) {
+  const uint64_t wave = static_cast<uint64_t>(sm_count()) * static_cast<uint64_t>(per_sm);
+  uint64_t g = stages < wave ? stages : wave;
+  return g < 1 ? 1 : g;
+}
+
+// Exact-sum partials of |W| into `partials`; returns their count in *n_partials.
+bl_status run_absum(const float* W, int64_t N, int64_t K, uint32_t* partials, int* n_partials, cudaStream_t s) {
+  static const int per_sm = ring_ctas_per_sm(reinterpret_cast<const void*>(bl::bl_absum_partials), bl::kAbsumThreads + 32);
+  if (per_sm <= 0) return fail(BL_ERR_CUDA, "bl_absum_partials: cannot reserve %u bytes of shared memory", bl::kRingSmem);
+  const uint64_t n4 = static_cast<uint64_t>(N) * static_cast<uint64_t>(K) / 4;
+  uint64_t ga = ring_grid((n4 + bl::kRingStageF4 - 1) / bl::kRingStageF4, per_sm);
+  if (ga > static_cast<uint64_t>(bl::kMaxAbsumCtas)) ga = bl::kMaxAbsumCtas;
+  cudaError_t e = bl::launch_pdl(bl::bl_absum_partials, dim3(static_cast<unsigned>(ga)), dim3(bl::kAbsumThreads + 32),
+                                 bl::kRingSmem, s, reinterpret_cast<const float4*>(W), n4, partials);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_absum_partials: %s", cudaGetErrorString(e));
+  *n_partials = static_cast<int>(ga);
+  return BL_OK;
 }
 
 bl_status run_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* workspace, cudaStream_t s) {
-  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
-  const uint64_t n4 = nk / 4;
-  const int sms = sm_count();
-  uint64_t ga = (n4 + bl::kAbsumThreads * 4 - 1) / (bl::kAbsumThreads * 4);
-  // one full wave: a second, partial wave of CTAs would trail the first
-  const uint64_t wave = static_cast<uint64_t>(sms) * static_cast<uint64_t>(absum_ctas_per_sm());
-  const uint64_t cap = wave < static_cast<uint64_t>(bl::kMaxAbsumCtas) ? wave : static_cast<uint64_t>(bl::kMaxAbsumCtas);
-  if (ga > cap) ga = cap;
-  if (ga < 1) ga = 1;
   uint32_t* partials = static_cast<uint32_t*>(workspace);
-  cudaError_t e = bl::launch_pdl(bl::bl_absum_partials, dim3(static_cast<unsigned>(ga)), dim3(bl::kAbsumThreads), 0, s,
-                                 reinterpret_cast<const float4*>(W), n4, partials);
-  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_absum_partials: %s", cudaGetErrorString(e));
-  e = bl::launch_pdl(bl::bl_gamma_finalize, dim3(1), dim3(256), 0, s, static_cast<const uint32_t*>(partials),
-                     static_cast<int>(ga), nk, gamma);
+  int n_partials = 0;
+  if (bl_status st = run_absum(W, N, K, partials, &n_partials, s)) return st;
+  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
+  cudaError_t e = bl::launch_pdl(bl::bl_gamma_finalize, dim3(1), dim3(256), 0, s, static_cast<const uint32_t*>(partials),
+                                 n_partials, nk, gamma);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gamma_finalize: %s", cudaGetErrorString(e));
   return BL_OK;
 }
 
-bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma, uint8_t* Wp, cudaStream_t s) {
-  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
-  const uint64_t n_bytes = nk / 4;
-  const uint64_t n_words = n_bytes / 4;
-  const int sms = sm_count();
-  static int per_sm = 0;   // resident CTAs of bl_quant_pack per SM: one full wave
-  if (per_sm == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, bl::bl_quant_pack, 256, 0) != cudaSuccess || n <= 0) n = 4;
-    per_sm = n;
-  }
-  uint64_t gq = (n_words + 255) / 256;
-  if (gq > static_cast<uint64_t>(sms) * per_sm) gq = static_cast<uint64_t>(sms) * per_sm;
-  if (gq < 1) gq = 1;
-  cudaError_t e = bl::launch_pdl(bl::bl_quant_pack, dim3(static_cast<unsigned>(gq)), dim3(256), 0, s,
-                                 reinterpret_cast<const float4*>(W), n_bytes, gamma, reinterpret_cast<uint32_t*>(Wp));
+// Codes and packing (see launch_quant_pack for the fused form).
+bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, float* gamma, const uint32_t* partials,
+                            int n_partials, uint8_t* Wp, cudaStream_t s) {
+  const uint64_t n_bytes = static_cast<uint64_t>(N) * static_cast<uint64_t>(K) / 4;
+  cudaError_t e = bl::launch_quant_pack(reinterpret_cast<const float4*>(W), n_bytes, gamma, partials, n_partials,
+                                        reinterpret_cast<uint32_t*>(Wp), sm_count(), s);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_quant_pack: %s", cudaGetErrorString(e));
   return BL_OK;
 }
@@ -294,7 +295,7 @@ bl_status bitlinear_quantize_pack(const float* W, int64_t N, int64_t K, const fl
   g_last_error.clear();
   if (bl_status st = check_pack_args(W, N, K, Wp, gamma)) return st;
   if (!Wp) return fail(BL_ERR_INVALID_ARG, "null pointer (Wp)");
-  return run_quantize_pack(W, N, K, gamma, Wp, reinterpret_cast<cudaStream_t>(stream));
+  return run_quantize_pack(W, N, K, const_cast<float*>(gamma), nullptr, 0, Wp, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, uint8_t* Wp, float* gamma,
@@ -304,8 +305,12 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, uint8_t* 
   if (!Wp) return fail(BL_ERR_INVALID_ARG, "null pointer (Wp)");
   if (bl_status st = check_pack_workspace(N, K, workspace, ws_bytes)) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (bl_status st = run_absmean(W, N, K, gamma, workspace, s)) return st;
-  return run_quantize_pack(W, N, K, gamma, Wp, s);
+  // gamma is combined inside the packing kernel, which starts streaming W
+  // while the exact sum finishes
+  uint32_t* partials = static_cast<uint32_t*>(workspace);
+  int n_partials = 0;
+  if (bl_status st = run_absum(W, N, K, partials, &n_partials, s)) return st;
+  return run_quantize_pack(W, N, K, gamma, partials, n_partials, Wp, s);
 }
 
 bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K, int8_t* xq, float* scale,

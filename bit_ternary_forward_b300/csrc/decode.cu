@@ -31,6 +31,7 @@
 //   sum_k field * x = sum_k code * x + sum_k x,
 // and the epilogue subtracts the per-token sum of x_q.
 
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -40,50 +41,8 @@ namespace {
 
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kTok = 8;                 // tokens per MMA column block
-constexpr uint32_t kWaitSpins = 1u << 26;
-
 // Set (never cleared by a kernel) when a bounded mbarrier wait gave up.
 __device__ int g_wait_error;
-
-BL_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-BL_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-BL_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-BL_DEVICE bool mbar_test(uint64_t* bar, uint32_t phase) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(phase)
-      : "memory");
-  return ok != 0u;
-}
-
-// Bounded wait: true once the phase completed, false after kWaitSpins polls.
-BL_DEVICE bool mbar_wait(uint64_t* bar, uint32_t phase) {
-  for (uint32_t i = 0; i < kWaitSpins; ++i) {
-    if (mbar_test(bar, phase)) return true;
-    if (i > 64) __nanosleep(64);
-  }
-  return false;
-}
-
-BL_DEVICE void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 BL_DEVICE void mma_u8s8(int (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -177,8 +136,7 @@ bl_decode_mma(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
   // ---- issue the weight copies (one thread), one mbarrier per 16-row tile
   if (tid == 0) {
     for (int tl = 0; tl < n_tiles; ++tl) mbar_init(&s_bar[tl], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_init_fence();
     for (int tl = 0; tl < n_tiles; ++tl) {
       const int r_lo = tl * 16, r_hi = min(R, r_lo + 16);
       mbar_expect_tx(&s_bar[tl], static_cast<uint32_t>((r_hi - r_lo) * rowbytes));

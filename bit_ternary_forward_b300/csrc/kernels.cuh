@@ -29,15 +29,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 bl_status record_error(bl_status st, const char* msg);
 
 // ---- weight packing (pack.cu)
-constexpr int kAbsumThreads = 256;
+// Both weight-pass kernels stream W through a ring of shared-memory stages
+// filled by bulk copies: consumer threads plus one producer warp.
+constexpr int kAbsumThreads = 512;          // consumers of the exact-sum kernel
+constexpr int kPackThreads = 256;           // consumers of the packing kernel
+constexpr int kRingStageF4 = 1024;          // float4 per stage (16 KB)
+constexpr int kRingStages = 6;              // stages in flight per CTA
+constexpr uint32_t kRingSmem = kRingStages * kRingStageF4 * 16;
+// Bytes of W the exact-sum pass marks to stay in L2 for the packing pass
+// (three quarters of a 126 MB L2).
+constexpr uint64_t kL2KeepBytes = 96ull << 20;
 constexpr int kPartialWords = 16;          // one 64-byte exact partial per CTA (12 limbs used)
 constexpr int kMaxAbsumCtas = 1184;        // 8 per SM on 148 SMs
 
 __global__ void bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials);
+cudaError_t take_pack_wait_error(int* flag);
 __global__ void bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_t count,
                                   float* __restrict__ gamma);
-__global__ void bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __restrict__ gamma,
-                              uint32_t* __restrict__ wp_words);
+// Codes and packing of W (n_bytes = N*K/4 output bytes) on a one-wave grid.
+// With partials (the fused form) every CTA combines gamma from the
+// exact-sum partials and CTA 0 writes it to *gamma; otherwise gamma is read.
+cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, float* gamma, const uint32_t* partials,
+                              int n_partials, uint32_t* wp_words, int sms, cudaStream_t s);
 
 // ---- activation quantisation (act_quant.cu)
 constexpr int kActThreads = 256;

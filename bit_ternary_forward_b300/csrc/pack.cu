@@ -33,6 +33,7 @@
 //      d = fp32(gamma + 1e-5), which equals clip(rint(fp32(w/d)), -1, 1) for
 //      every finite w (see ternary_field in common.cuh).
 
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -43,14 +44,6 @@ namespace {
 constexpr int kLimbs = 12;            // 384-bit fixed point, units of 2^-149
 constexpr int kSmemLimbs = 16;        // headroom for shifted pieces
 constexpr int kBins = 256;
-
-// Streaming 16-byte load that does not allocate in L1.
-BL_DEVICE float4 ld_f4_stream(const float4* p) {
-  float4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-  return v;
-}
 
 // (a2:a1:a0) += (hi:lo), 96-bit, carries through the flag register.
 BL_DEVICE void add96(uint32_t& a0, uint32_t& a1, uint32_t& a2, uint32_t lo, uint32_t hi) {
@@ -85,13 +78,6 @@ BL_DEVICE void add_words_shifted(unsigned long long* limbs, const uint32_t (&w)[
 
 BL_DEVICE int exp_field(float x) { return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu); }
 
-// a << s with PTX semantics: shift amounts of 32 or more give 0.
-BL_DEVICE uint32_t shl_clamped(uint32_t a, uint32_t s) {
-  uint32_t r;
-  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(s));
-  return r;
-}
-
 // a * b + c with a 64-bit addend and result (exact while it stays below 2^64).
 BL_DEVICE unsigned long long mad_wide_u32(uint32_t a, uint32_t b, unsigned long long c) {
   unsigned long long r;
@@ -101,97 +87,142 @@ BL_DEVICE unsigned long long mad_wide_u32(uint32_t a, uint32_t b, unsigned long 
 
 }  // namespace
 
-__global__ void __launch_bounds__(kAbsumThreads)
+// Set (never cleared by a kernel) when a bounded mbarrier wait gave up.
+__device__ int g_pack_wait_error;
+
+// 1 << (s mod 32): funnel shift of (1:0) with wrap-around shift amounts.
+BL_DEVICE uint32_t pow2_wrap(uint32_t s) {
+  uint32_t r;
+  asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(0u), "r"(1u), "r"(s));
+  return r;
+}
+
+__global__ void __launch_bounds__(kAbsumThreads + 32, 2)
 bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials) {
+  extern __shared__ __align__(128) float4 s_ring[];        // kRingStages x kRingStageF4
   __shared__ unsigned long long s_bins[kBins];
   __shared__ unsigned long long s_limbs[kSmemLimbs];
+  __shared__ __align__(8) uint64_t s_full[kRingStages], s_empty[kRingStages];
+  constexpr int kConsumerWarps = kAbsumThreads / 32;
+  constexpr int kPer = kRingStageF4 / kAbsumThreads;      // float4 per consumer thread and stage
+  // a fold adds kPer * 4 window terms below 2^55 each: far below 2^64
+  static_assert(kPer * kAbsumThreads == kRingStageF4 && kPer * 4 <= 256, "fold bound");
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kBins; i += blockDim.x) s_bins[i] = 0ull;
   if (tid < kSmemLimbs) s_limbs[tid] = 0ull;
-
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  const uint64_t first = static_cast<uint64_t>(blockIdx.x) * blockDim.x + tid;
-  auto ld_stream_f4 = [](const float4* p) { return ld_f4_stream(p); };
+  if (tid == 0) {
+    for (int s = 0; s < kRingStages; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kConsumerWarps);
+    }
+    mbar_init_fence();
+  }
+  // this CTA's share: the contiguous float4 range [f0, f1), in stages of
+  // kRingStageF4 (the last one shorter)
+  const uint64_t f0 = n4 * blockIdx.x / gridDim.x, f1 = n4 * (blockIdx.x + 1) / gridDim.x;
+  const int n_stages = static_cast<int>((f1 - f0 + kRingStageF4 - 1) / kRingStageF4);
+  __syncthreads();   // barriers initialised, bins and limbs cleared
   pdl_wait();
   pdl_launch_dependents();
   w4 = launder(w4);
+  bool ok = true;
 
-  // Warp-uniform window [base, base + 31] in units of 2^-149; a normal weight
-  // with exponent field e and significand m (implicit bit included) is
-  // m * 2^(e - 1) in those units, so d = e - 1 - base.
-  float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (first < n4) v0 = ld_stream_f4(w4 + first);
-  int e_loc = max(max(exp_field(v0.x), exp_field(v0.y)), max(exp_field(v0.z), exp_field(v0.w)));
-  e_loc = min(e_loc, 254);
-  const int e_max = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(e_loc)));
-  const int top = min(max(e_max - 1, 0) + 4, 253);
-  const int base = max(0, top - 31);
-  const uint32_t bias = static_cast<uint32_t>(base) + 1u;
-  __syncthreads();   // bins and limbs cleared
+  uint32_t a0 = 0u, a1 = 0u, a2 = 0u;      // 96-bit total of this thread
+  int base = 0;                            // warp-uniform window bottom, units of 2^-149
 
-  uint32_t a0 = 0u, a1 = 0u, a2 = 0u;      // 96-bit total
-  unsigned long long acc = 0ull;           // at most 16 window terms below 2^55 each
-
-  // out-of-window weights of a float4 (rare): exact per-exponent bins
-  auto rare = [&](float x) {
-    const uint32_t b = __float_as_uint(x) & 0x7fffffffu;
-    const uint32_t e = b >> 23;
-    if ((e - bias) >= 32u && b != 0u) {
-      const uint32_t m = e ? ((b & 0x7fffffu) | 0x800000u) : b;
-      atomicAdd(&s_bins[e ? e - 1u : 0u], static_cast<unsigned long long>(m));
+  if (warp == kConsumerWarps) {
+    // ---- producer: one thread keeps kRingStages bulk copies in flight
+    // W is read again by the packing pass: the first kL2KeepBytes of it stay
+    // in L2 at high priority, the rest streams through
+    if (lane == 0)
+      ok = ring_produce(s_ring, kRingStageF4 * 16u, kRingStages, w4 + f0, (f1 - f0) * 16u, s_full, s_empty,
+                        f0 * 16u < kL2KeepBytes ? l2_evict_last() : l2_evict_first());
+    __syncwarp();
+  } else {
+    // ---- consumers: thread t sums float4 t, t + kAbsumThreads, ... of every stage
+    uint32_t bias = 0u;
+    // out-of-window weights of a float4 (rare): exact per-exponent bins
+    auto rare = [&](float x) {
+      const uint32_t b = __float_as_uint(x) & 0x7fffffffu;
+      const uint32_t e = b >> 23;
+      if ((e - bias) >= 32u && b != 0u) {
+        const uint32_t m = e ? ((b & 0x7fffffu) | 0x800000u) : b;
+        atomicAdd(&s_bins[e ? e - 1u : 0u], static_cast<unsigned long long>(m));
+      }
+    };
+    // Window terms of a float4 into acc. With the sign bit left in, the shift
+    // amount (bits >> 23) - bias is the binade distance plus 256 for a
+    // negative weight; 256 is a multiple of 32, so the wrapping shift gives
+    // the same power of two, and a weight lies in the window iff bits 5..7
+    // of that amount are clear (for either sign, and for any wrapped value).
+    auto take4 = [&](const float4& v, unsigned long long& acc) {
+      const uint32_t b0 = __float_as_uint(v.x), b1 = __float_as_uint(v.y);
+      const uint32_t b2 = __float_as_uint(v.z), b3 = __float_as_uint(v.w);
+      const uint32_t d0 = (b0 >> 23) - bias, d1 = (b1 >> 23) - bias, d2 = (b2 >> 23) - bias, d3 = (b3 >> 23) - bias;
+      acc = mad_wide_u32((b0 & 0x7fffffu) | 0x800000u, pow2_wrap(d0), acc);
+      acc = mad_wide_u32((b1 & 0x7fffffu) | 0x800000u, pow2_wrap(d1), acc);
+      acc = mad_wide_u32((b2 & 0x7fffffu) | 0x800000u, pow2_wrap(d2), acc);
+      acc = mad_wide_u32((b3 & 0x7fffffu) | 0x800000u, pow2_wrap(d3), acc);
+      if ((d0 | d1 | d2 | d3) & 0xe0u) {
+        // the four window terms above are exact only for in-window weights:
+        // take back those of the others and bin them instead
+        const uint32_t dd[4] = {d0, d1, d2, d3};
+        const uint32_t bb[4] = {b0, b1, b2, b3};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (dd[q] & 0xe0u) acc -= static_cast<unsigned long long>((bb[q] & 0x7fffffu) | 0x800000u) << (dd[q] & 31u);
+        rare(v.x); rare(v.y); rare(v.z); rare(v.w);
+      }
+    };
+    for (int j = 0; j < n_stages; ++j) {
+      const int s = j % kRingStages;
+      // warp-uniform verdict, so a timed-out lane cannot split the warp
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (j / kRingStages) & 1))) {
+        ok = false;
+        break;
+      }
+      const float4* st = s_ring + s * kRingStageF4;
+      const uint64_t lo = f0 + static_cast<uint64_t>(j) * kRingStageF4;
+      const int cnt = static_cast<int>(min(f1 - lo, static_cast<uint64_t>(kRingStageF4)));
+      if (j == 0) {
+        // Warp-uniform window [base, base + 31] from the largest exponent
+        // among the warp's first 128 weights; a normal weight with exponent
+        // field e and significand m (implicit bit included) is m * 2^(e - 1)
+        // in units of 2^-149, so its distance above the bottom is e - 1 - base.
+        const float4 v0 = tid < cnt ? st[tid] : make_float4(0.f, 0.f, 0.f, 0.f);
+        int e_loc = max(max(exp_field(v0.x), exp_field(v0.y)), max(exp_field(v0.z), exp_field(v0.w)));
+        e_loc = min(e_loc, 254);
+        const int e_max = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(e_loc)));
+        const int top = min(max(e_max - 1, 0) + 4, 253);
+        base = max(0, top - 31);
+        bias = static_cast<uint32_t>(base) + 1u;
+      }
+      unsigned long long acc[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) acc[k] = 0ull;
+      if (cnt == kRingStageF4) {
+        float4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) v[k] = st[tid + k * kAbsumThreads];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) take4(v[k], acc[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < kPer; ++k)
+          if (tid + k * kAbsumThreads < cnt) take4(st[tid + k * kAbsumThreads], acc[k]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[s]);
+      unsigned long long t = acc[0];
+#pragma unroll
+      for (int k = 1; k < kPer; ++k) t += acc[k];
+      add96(a0, a1, a2, static_cast<uint32_t>(t), static_cast<uint32_t>(t >> 32));
     }
-  };
-  auto take4 = [&](const float4& v) {
-    const uint32_t b0 = __float_as_uint(v.x) & 0x7fffffffu, b1 = __float_as_uint(v.y) & 0x7fffffffu;
-    const uint32_t b2 = __float_as_uint(v.z) & 0x7fffffffu, b3 = __float_as_uint(v.w) & 0x7fffffffu;
-    const uint32_t d0 = (b0 >> 23) - bias, d1 = (b1 >> 23) - bias, d2 = (b2 >> 23) - bias, d3 = (b3 >> 23) - bias;
-    acc = mad_wide_u32((b0 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d0), acc);
-    acc = mad_wide_u32((b1 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d1), acc);
-    acc = mad_wide_u32((b2 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d2), acc);
-    acc = mad_wide_u32((b3 & 0x7fffffu) | 0x800000u, shl_clamped(1u, d3), acc);
-    if ((d0 | d1 | d2 | d3) >= 32u) {
-      rare(v.x); rare(v.y); rare(v.z); rare(v.w);
-    }
-  };
-  auto fold = [&]() {
-    add96(a0, a1, a2, static_cast<uint32_t>(acc), static_cast<uint32_t>(acc >> 32));
-    acc = 0ull;
-  };
+  }
+  if (!ok) atomicExch(&g_pack_wait_error, 1);
 
-  if (first < n4) {
-    take4(v0);
-    fold();
-  }
-  // software pipeline: the next four float4 of this thread are in flight while
-  // the current four are summed
-  uint64_t i = first + stride;
-  float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0, c2 = c0, c3 = c0;
-  bool have = i + 3 * stride < n4;
-  if (have) {
-    c0 = ld_stream_f4(w4 + i); c1 = ld_stream_f4(w4 + i + stride);
-    c2 = ld_stream_f4(w4 + i + 2 * stride); c3 = ld_stream_f4(w4 + i + 3 * stride);
-  }
-  while (have) {
-    const uint64_t nxt = i + 4 * stride;
-    const bool more = nxt + 3 * stride < n4;
-    float4 p0 = c0, p1 = c1, p2 = c2, p3 = c3;
-    if (more) {
-      p0 = ld_stream_f4(w4 + nxt); p1 = ld_stream_f4(w4 + nxt + stride);
-      p2 = ld_stream_f4(w4 + nxt + 2 * stride); p3 = ld_stream_f4(w4 + nxt + 3 * stride);
-    }
-    take4(c0); take4(c1); take4(c2); take4(c3);
-    fold();
-    c0 = p0; c1 = p1; c2 = p2; c3 = p3;
-    i = nxt;
-    have = more;
-  }
-  for (; i < n4; i += stride) {
-    take4(ld_stream_f4(w4 + i));
-    fold();
-  }
-
-  // warp sum of the 96-bit accumulators (all lanes share `base`)
+  // warp sum of the 96-bit accumulators (all lanes of a warp share `base`)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const uint32_t b0 = __shfl_down_sync(0xffffffffu, a0, o);
@@ -200,7 +231,7 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
     add96(a0, a1, a2, b0, b1, b2);
   }
   __syncthreads();   // every bin update done
-  if ((tid & 31) == 0) {
+  if (lane == 0 && warp < kConsumerWarps) {
     const uint32_t w[3] = {a0, a1, a2};
     add_words_shifted(s_limbs, w, base);
   }
@@ -224,59 +255,26 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
   }
 }
 
-__global__ void __launch_bounds__(256)
-bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_t count,
-                  float* __restrict__ gamma) {
-  __shared__ unsigned long long s_part[256 / 32][kLimbs];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
-  pdl_launch_dependents();
-  partials = launder(partials);
-  unsigned long long loc[kLimbs];
-#pragma unroll
-  for (int l = 0; l < kLimbs; ++l) loc[l] = 0ull;
-  for (int c = tid; c < n_partials; c += blockDim.x) {
-    const uint4* p = reinterpret_cast<const uint4*>(partials + static_cast<size_t>(c) * kPartialWords);
-    const uint4 q0 = p[0], q1 = p[1], q2 = p[2];
-    loc[0] += q0.x; loc[1] += q0.y; loc[2] += q0.z; loc[3] += q0.w;
-    loc[4] += q1.x; loc[5] += q1.y; loc[6] += q1.z; loc[7] += q1.w;
-    loc[8] += q2.x; loc[9] += q2.y; loc[10] += q2.z; loc[11] += q2.w;
-  }
-#pragma unroll
-  for (int l = 0; l < kLimbs; ++l) {
-    unsigned long long v = loc[l];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
-    if (lane == 0) s_part[warp][l] = v;
-  }
-  __syncthreads();
-  // limb l summed over the warps by thread l: 32-bit halves kept apart so no
-  // 64-bit sum can wrap (each warp value is below 2^32 * n_partials)
-  __shared__ unsigned long long s_lo[kLimbs], s_hi[kLimbs];
-  if (tid < kLimbs) {
-    unsigned long long lo = 0, hi = 0;
-#pragma unroll
-    for (int w = 0; w < 256 / 32; ++w) {
-      lo += s_part[w][tid] & 0xffffffffull;
-      hi += s_part[w][tid] >> 32;
-    }
-    s_lo[tid] = lo;
-    s_hi[tid] = hi;
-  }
-  __syncthreads();
-  if (tid != 0) return;
+cudaError_t take_pack_wait_error(int* flag) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flag, g_pack_wait_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_pack_wait_error, &zero, sizeof(int));
+}
 
-  // exact sum S in 32-bit limbs (S < 2^309)
-  uint32_t S[kLimbs + 1];
-  unsigned long long carry = 0;
-#pragma unroll
-  for (int l = 0; l < kLimbs; ++l) {
-    const unsigned long long v = carry + s_lo[l];
-    S[l] = static_cast<uint32_t>(v);
-    carry = (v >> 32) + s_hi[l];
-  }
-  S[kLimbs] = static_cast<uint32_t>(carry);
+namespace {
 
+constexpr int kFinalThreads = 256;      // threads that combine the partials
+
+struct FinalSmem {
+  unsigned long long part[kFinalThreads / 32][kLimbs];
+  unsigned long long lo[kLimbs], hi[kLimbs];
+  float gamma;
+};
+
+// Exact sum S (32-bit limbs, units of 2^-149) divided by count and rounded
+// once to fp32, ties to even.
+BL_DEVICE float round_mean(const uint32_t (&S)[kLimbs + 1], uint64_t count) {
   // T = the top 64 bits of S (all of S when it is shorter), sh = bits dropped
   int topl = kLimbs;
   while (topl > 0 && S[topl] == 0u) --topl;
@@ -315,64 +313,194 @@ bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_
   }
   unsigned long long bits = (static_cast<unsigned long long>(t) << 23) + mant + (up ? 1ull : 0ull);
   if (bits >= 0x7f800000ull) bits = 0x7f800000ull;   // unreachable for finite inputs
-  *gamma = __uint_as_float(static_cast<uint32_t>(bits));
+  return __uint_as_float(static_cast<uint32_t>(bits));
 }
 
-// 16 weights -> 4 packed bytes (one 32-bit word).
-BL_DEVICE uint32_t pack16(const float4& a, const float4& b, const float4& c, const float4& d, float h) {
-  uint32_t r = 0;
-  r |= ternary_field(a.x, h) << 0;  r |= ternary_field(a.y, h) << 2;
-  r |= ternary_field(a.z, h) << 4;  r |= ternary_field(a.w, h) << 6;
-  r |= ternary_field(b.x, h) << 8;  r |= ternary_field(b.y, h) << 10;
-  r |= ternary_field(b.z, h) << 12; r |= ternary_field(b.w, h) << 14;
-  r |= ternary_field(c.x, h) << 16; r |= ternary_field(c.y, h) << 18;
-  r |= ternary_field(c.z, h) << 20; r |= ternary_field(c.w, h) << 22;
-  r |= ternary_field(d.x, h) << 24; r |= ternary_field(d.y, h) << 26;
-  r |= ternary_field(d.z, h) << 28; r |= ternary_field(d.w, h) << 30;
-  return r;
+// gamma from the exact per-CTA partials, run by threads 0 .. kFinalThreads - 1
+// of the CTA; sync() is a barrier over exactly those threads. Every caller
+// thread gets gamma.
+template <typename Sync>
+BL_DEVICE float gamma_from_partials(const uint32_t* partials, int n_partials, uint64_t count, FinalSmem& sm,
+                                    Sync sync) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long loc[kLimbs];
+#pragma unroll
+  for (int l = 0; l < kLimbs; ++l) loc[l] = 0ull;
+  for (int c = tid; c < n_partials; c += kFinalThreads) {
+    const uint4* p = reinterpret_cast<const uint4*>(partials + static_cast<size_t>(c) * kPartialWords);
+    const uint4 q0 = p[0], q1 = p[1], q2 = p[2];
+    loc[0] += q0.x; loc[1] += q0.y; loc[2] += q0.z; loc[3] += q0.w;
+    loc[4] += q1.x; loc[5] += q1.y; loc[6] += q1.z; loc[7] += q1.w;
+    loc[8] += q2.x; loc[9] += q2.y; loc[10] += q2.z; loc[11] += q2.w;
+  }
+#pragma unroll
+  for (int l = 0; l < kLimbs; ++l) {
+    unsigned long long v = loc[l];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+    if (lane == 0) sm.part[warp][l] = v;
+  }
+  sync();
+  // limb l summed over the warps by thread l: 32-bit halves kept apart so no
+  // 64-bit sum can wrap (each warp value is below 2^32 * n_partials)
+  if (tid < kLimbs) {
+    unsigned long long lo = 0, hi = 0;
+#pragma unroll
+    for (int w = 0; w < kFinalThreads / 32; ++w) {
+      lo += sm.part[w][tid] & 0xffffffffull;
+      hi += sm.part[w][tid] >> 32;
+    }
+    sm.lo[tid] = lo;
+    sm.hi[tid] = hi;
+  }
+  sync();
+  if (tid == 0) {
+    // exact sum S in 32-bit limbs (S < 2^309)
+    uint32_t S[kLimbs + 1];
+    unsigned long long carry = 0;
+#pragma unroll
+    for (int l = 0; l < kLimbs; ++l) {
+      const unsigned long long v = carry + sm.lo[l];
+      S[l] = static_cast<uint32_t>(v);
+      carry = (v >> 32) + sm.hi[l];
+    }
+    S[kLimbs] = static_cast<uint32_t>(carry);
+    sm.gamma = round_mean(S, count);
+  }
+  sync();
+  return sm.gamma;
 }
 
-__global__ void __launch_bounds__(256)
-bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __restrict__ gamma,
-              uint32_t* __restrict__ wp_words) {
-  const uint64_t n_words = n_bytes >> 2;
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+}  // namespace
+
+__global__ void __launch_bounds__(kFinalThreads)
+bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_t count,
+                  float* __restrict__ gamma) {
+  __shared__ FinalSmem sm;
   pdl_wait();
   pdl_launch_dependents();
-  w4 = launder(w4);
-  gamma = launder(gamma);
-  // software pipeline: the next word's 16 weights load while this one packs,
-  // and the first loads are in flight before gamma arrives
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, c = a, e = a;
-  if (i < n_words) {
-    const float4* src = w4 + 4 * i;
-    a = ld_f4_stream(src); b = ld_f4_stream(src + 1);
-    c = ld_f4_stream(src + 2); e = ld_f4_stream(src + 3);
-  }
-  const float d = __fadd_rn(*gamma, kEpsGamma);
-  const float h = 0.5f * d;                 // exact: d is a normal fp32
-  while (i < n_words) {
-    const uint64_t nxt = i + stride;
-    float4 na = a, nb = b, nc = c, ne = e;
-    if (nxt < n_words) {
-      const float4* src = w4 + 4 * nxt;
-      na = ld_f4_stream(src); nb = ld_f4_stream(src + 1);
-      nc = ld_f4_stream(src + 2); ne = ld_f4_stream(src + 3);
+  partials = launder(partials);
+  const float g = gamma_from_partials(partials, n_partials, count, sm, [] { __syncthreads(); });
+  if (threadIdx.x == 0) *gamma = g;
+}
+
+// Four weights -> one packed byte (fields in bits 0-1, 2-3, 4-5, 6-7).
+BL_DEVICE uint32_t pack4(const float4& v, float h) {
+  return ternary_field(v.x, h) | (ternary_field(v.y, h) << 2) | (ternary_field(v.z, h) << 4) |
+         (ternary_field(v.w, h) << 6);
+}
+
+template <bool FUSED>
+__global__ void __launch_bounds__(kPackThreads + 32, 2)
+bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __restrict__ gamma_in,
+              const uint32_t* __restrict__ partials, int n_partials, float* __restrict__ gamma_out,
+              uint32_t* __restrict__ wp_words) {
+  extern __shared__ __align__(128) float4 s_ring[];        // kRingStages x kRingStageF4
+  __shared__ __align__(8) uint64_t s_full[kRingStages], s_empty[kRingStages];
+  __shared__ FinalSmem s_fin;
+  constexpr int kConsumerWarps = kPackThreads / 32;
+  constexpr int kStageWords = kRingStageF4 / 4;            // packed words per stage
+  static_assert(kStageWords == kPackThreads, "one packed word per consumer thread and stage");
+  static_assert(kPackThreads == kFinalThreads, "the consumers combine the partials");
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int s = 0; s < kRingStages; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kConsumerWarps);
     }
-    wp_words[i] = pack16(a, b, c, e, h);
-    a = na; b = nb; c = nc; e = ne;
-    i = nxt;
+    mbar_init_fence();
   }
-  // tail: up to three bytes when N*K/4 is not a multiple of 4
-  const uint64_t t = (static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x);
-  const uint64_t tb = n_words * 4 + t;
-  if (tb < n_bytes) {
-    float4 v = w4[tb];
-    uint8_t* wp = reinterpret_cast<uint8_t*>(wp_words);
-    wp[tb] = static_cast<uint8_t>(ternary_field(v.x, h) | (ternary_field(v.y, h) << 2) |
-                                  (ternary_field(v.z, h) << 4) | (ternary_field(v.w, h) << 6));
+  // this CTA's share: the contiguous word range [q0, q1); word q packs the 16
+  // weights of float4 4q .. 4q + 3
+  const uint64_t n_words = n_bytes >> 2;
+  const uint64_t q0 = n_words * blockIdx.x / gridDim.x, q1 = n_words * (blockIdx.x + 1) / gridDim.x;
+  const int n_stages = static_cast<int>((q1 - q0 + kStageWords - 1) / kStageWords);
+  __syncthreads();
+  bool ok = true;
+
+  if (warp == kConsumerWarps) {
+    // The producer of the fused form streams W before the dependency wait:
+    // its predecessor is the exact-sum kernel of the same W, which reads W
+    // only and released this grid after its own dependency wait, so every
+    // earlier write of W is complete and visible by now. The stand-alone
+    // form cannot know who wrote W last and waits first.
+    if (!FUSED) pdl_wait();
+    if (lane == 0)
+      ok = ring_produce(s_ring, kRingStageF4 * 16u, kRingStages, launder(w4) + 4 * q0, (q1 - q0) * 64u, s_full,
+                        s_empty, l2_evict_first());   // the last read of W
+    __syncwarp();
+  } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    float g;
+    if (FUSED) {
+      // every CTA combines the partials itself (while its first stages are in
+      // flight); CTA 0 publishes gamma
+      g = gamma_from_partials(launder(partials), n_partials, n_bytes * 4, s_fin,
+                              [] { asm volatile("bar.sync 1, %0;" ::"n"(kPackThreads) : "memory"); });
+      if (blockIdx.x == 0 && tid == 0) *gamma_out = g;
+    } else {
+      g = *launder(gamma_in);
+    }
+    const float d = __fadd_rn(g, kEpsGamma);
+    const float h = 0.5f * d;                 // exact: d is a normal fp32
+    // Thread t packs word t of each stage from float4 4t .. 4t + 3, taking
+    // them in the rotated order (k + t/2) mod 4, so that the eight threads of
+    // each quarter-warp read eight different 16-byte bank groups.
+    const int rot = (tid >> 1) & 3;
+    for (int j = 0; j < n_stages; ++j) {
+      const int s = j % kRingStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (j / kRingStages) & 1))) {
+        ok = false;
+        break;
+      }
+      const uint64_t w0 = q0 + static_cast<uint64_t>(j) * kStageWords;
+      const bool mine = w0 + tid < q1;
+      const float4* st = s_ring + s * kRingStageF4 + 4 * tid;
+      uint32_t r = 0u;
+      if (mine) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int q = (k + rot) & 3;
+          r |= pack4(st[q], h) << (8 * q);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[s]);
+      if (mine) wp_words[w0 + tid] = r;
+    }
+    // tail: up to three bytes when N*K/4 is not a multiple of 4
+    const uint64_t tb = n_words * 4 + static_cast<uint64_t>(blockIdx.x) * kPackThreads + tid;
+    if (tb < n_bytes) reinterpret_cast<uint8_t*>(wp_words)[tb] = static_cast<uint8_t>(pack4(launder(w4)[tb], h));
   }
+  if (!ok) atomicExch(&g_pack_wait_error, 1);
+}
+
+cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, float* gamma, const uint32_t* partials,
+                              int n_partials, uint32_t* wp_words, int sms, cudaStream_t s) {
+  const bool fused = partials != nullptr;
+  auto kern = fused ? bl_quant_pack<true> : bl_quant_pack<false>;
+  // resident CTAs per SM of each form (0: the shared memory cannot be reserved)
+  auto per_sm_of = [](const void* k) {
+    int n = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRingSmem)) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kPackThreads + 32, kRingSmem) != cudaSuccess)
+      n = 0;
+    return n;
+  };
+  static const int per_sm_plain = per_sm_of(reinterpret_cast<const void*>(bl_quant_pack<false>));
+  static const int per_sm_fused = per_sm_of(reinterpret_cast<const void*>(bl_quant_pack<true>));
+  const int per_sm = fused ? per_sm_fused : per_sm_plain;
+  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  const uint64_t n_words = n_bytes / 4;
+  const uint64_t stages = (n_words + kRingStageF4 / 4 - 1) / (kRingStageF4 / 4);
+  const uint64_t wave = static_cast<uint64_t>(sms) * static_cast<uint64_t>(per_sm);
+  uint64_t grid = stages < wave ? stages : wave;
+  if (grid < 1) grid = 1;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kPackThreads + 32), kRingSmem, s, w4, n_bytes,
+                    static_cast<const float*>(gamma), partials, n_partials, gamma, wp_words);
 }
 
 }  // namespace bl

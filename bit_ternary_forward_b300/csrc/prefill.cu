@@ -49,6 +49,7 @@
 #include <cuda_fp16.h>
 #include <mutex>
 
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -83,41 +84,7 @@ constexpr int stages_for(int bn) {
 constexpr uint32_t smem_for(int bn) {
   return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + kEStages * kWeBytes + kMiscBytes + 1024;
 }
-constexpr uint32_t kWaitTries = 1u << 16;
-
 __device__ int g_tc_wait_error;
-
-BL_DEVICE uint32_t smem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-BL_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-BL_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-BL_DEVICE void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-// One bounded-time wait: the hardware suspends the thread until the phase
-// completes or a system-dependent time limit passes.
-BL_DEVICE bool mbar_try(uint64_t* bar, uint32_t phase) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(phase)
-      : "memory");
-  return ok != 0u;
-}
-// Bounded wait: true once the phase completed, false after kWaitTries
-// suspended waits (each ends by itself), so a lost arrival cannot hang.
-BL_DEVICE bool mbar_wait(uint64_t* bar, uint32_t phase) {
-  for (uint32_t i = 0; i < kWaitTries; ++i)
-    if (mbar_try(bar, phase)) return true;
-  return false;
-}
 
 BL_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
@@ -236,8 +203,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),

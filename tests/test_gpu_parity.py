@@ -128,6 +128,26 @@ def test_activation_ties_on_device():
     assert xq.cpu().tolist() == [[2, 4, 0, 126, 127, -2, 0, -2]]
 
 
+# ------------------------------------------------------------------ the stand-alone packing calls
+@pytest.mark.parametrize("n,k", [(1, 4), (3, 12), (7, 1028), (256, 1024), (1000, 1028), (2048, 2052)])
+def test_absmean_then_quantize_pack_match_pack_weights(n, k):
+    """bitlinear_absmean + bitlinear_quantize_pack (gamma read from memory) and
+    bitlinear_pack_weights (gamma combined inside the packing kernel) both
+    give the oracle's gamma and bytes: one-byte and one-word outputs, tails
+    of 1..3 bytes, and grids with several ring stages per CTA."""
+    w = gaussian_weights(n, k, seed=n + k)
+    g_ref, _, wp_ref = oracle_weights(w)
+    wd = w.cuda()
+    gamma = blt.absmean(wd)
+    wp = blt.quantize_pack(wd, gamma)
+    packed = blt.pack_weights(wd)
+    torch.cuda.synchronize()
+    assert bits(gamma.cpu().numpy()[0]) == bits(g_ref)
+    assert bits(packed.gamma.cpu().numpy()[0]) == bits(g_ref)
+    np.testing.assert_array_equal(wp.cpu().numpy(), wp_ref)
+    np.testing.assert_array_equal(packed.wp.cpu().numpy(), wp_ref)
+
+
 # ------------------------------------------------------------------ invariants of the device path
 def test_pack_is_deterministic_and_order_free():
     w = gaussian_weights(512, 1024, seed=15)
