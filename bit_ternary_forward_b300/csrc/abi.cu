@@ -106,15 +106,22 @@ size_t small_workspace_bytes(int64_t M, int64_t K) {
   return align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256) + 2 * align_up(static_cast<size_t>(M) * 4, 256);
 }
 
-// Workspace of the tensor-core path: fp16 operand, token sums, scales.
+// Workspace of the tensor-core path: fp16 operand, token sums, scales, then
+// the contraction's split-tile buffer and counters.
 struct TcWorkspace {
   void* xperm;
   int* rowsum;
   float* scale;
+  void* sk;
 };
 
-size_t tc_workspace_bytes(int64_t M, int64_t K) {
-  return align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2, 256) + 2 * align_up(static_cast<size_t>(M) * 4, 256);
+bl::TcPlan tc_plan_for(int64_t M, int64_t N, int64_t K) {
+  return bl::tc_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sm_count());
+}
+
+size_t tc_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return align_up(static_cast<size_t>(M) * static_cast<size_t>(K) * 2, 256) +
+         2 * align_up(static_cast<size_t>(M) * 4, 256) + tc_plan_for(M, N, K).sk_bytes;
 }
 
 TcWorkspace tc_workspace(void* ws, int64_t M, int64_t K) {
@@ -125,6 +132,8 @@ TcWorkspace tc_workspace(void* ws, int64_t M, int64_t K) {
   t.rowsum = reinterpret_cast<int*>(b);
   b += align_up(static_cast<size_t>(M) * 4, 256);
   t.scale = reinterpret_cast<float*>(b);
+  b += align_up(static_cast<size_t>(M) * 4, 256);
+  t.sk = b;
   return t;
 }
 
@@ -132,12 +141,13 @@ bl_status run_tc(const void* x, int xin, const float* scale_in, const uint8_t* W
                  bool out_acc, int8_t* xq_out, float* scale_out, int64_t M, int64_t N, int64_t K, void* ws,
                  cudaStream_t s) {
   TcWorkspace t = tc_workspace(ws, M, K);
+  const bl::TcPlan plan = tc_plan_for(M, N, K);
   float* sc = xin == bl::kXinI8 ? const_cast<float*>(scale_in) : (scale_out ? scale_out : t.scale);
   cudaError_t e = bl::launch_act_perm(x, xin, scale_in, static_cast<int>(M), static_cast<int>(K), xq_out,
-                                      xin == bl::kXinI8 ? nullptr : sc, t.xperm, t.rowsum, s);
+                                      xin == bl::kXinI8 ? nullptr : sc, t.xperm, t.rowsum, t.sk, plan.sk_bytes, s);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_act_perm: %s", cudaGetErrorString(e));
   e = bl::launch_gemm_tc(t.xperm, Wp, sc, t.rowsum, gamma, out, out_acc, static_cast<int>(M), static_cast<int>(N),
-                         static_cast<int>(K), s);
+                         static_cast<int>(K), plan, t.sk, s);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemm_tc: %s", cudaGetErrorString(e));
   return BL_OK;
 }
@@ -325,9 +335,8 @@ bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K, 
 }
 
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
-  if (M <= 0 || K <= 0) return 0;
-  if (use_tc(M, K)) return tc_workspace_bytes(M, K);
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (use_tc(M, K)) return tc_workspace_bytes(M, N, K);
   return small_workspace_bytes(M, K);
 }
 
@@ -365,8 +374,8 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
 }
 
 size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || K <= 0) return 0;
-  if (use_tc(M, K)) return tc_workspace_bytes(M, K);
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if (use_tc(M, K)) return tc_workspace_bytes(M, N, K);
   if (gemv_plan(M, N, K).smem) return small_workspace_bytes(M, K);
   return 0;
 }

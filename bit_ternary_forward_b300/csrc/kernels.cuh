@@ -108,15 +108,28 @@ cudaError_t take_gemv_wait_error(int* flag);
 // ---- prefill contraction on tcgen05 (prefill.cu)
 constexpr int kTcMinM = 65;   // smallest M routed to the tensor-core kernel
 size_t gemm_tc_smem_bytes();
+// Launch plan of the tensor-core contraction (tc_plan, prefill.cu): token-tile
+// width, grid, whole tiles and split ("stream-K") tiles, and the bytes of its
+// split-tile workspace (an fp32 buffer of sk_buf_bytes, then int counters),
+// which must be zero when the contraction starts.
+struct TcPlan {
+  int bn = 256, grid = 1, n_tiles_n = 1, k_iters = 1, dp_tiles = 0, sk_tiles = 0, sk_ctas = 0;
+  size_t sk_buf_bytes = 0, sk_bytes = 0;
+};
+TcPlan tc_plan(int M, int N, int K, int sms);
 // x (fp32 / bf16, or int8 x_q with xin == kXinI8) -> fp16 operand xperm [M][K]
 // (transposed 16-code blocks scaled by 4^-i), token sums rowsum [M], and for
-// float input the scales scale_out [M] and optionally int8 codes xq_out.
+// float input the scales scale_out [M] and optionally int8 codes xq_out; also
+// zeroes zero_bytes (a multiple of 16) at `zero`.
 cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M, int K, int8_t* xq_out,
-                            float* scale_out, void* xperm, int* rowsum, cudaStream_t s);
+                            float* scale_out, void* xperm, int* rowsum, void* zero, size_t zero_bytes,
+                            cudaStream_t s);
 // y (or int32 acc when out_acc) from xperm, rowsum, scale and packed weights;
-// needs K % 64 == 0. Returns cudaErrorNotSupported if tensor maps cannot be made.
+// needs K % 64 == 0; sk_ws is the plan's zeroed split-tile workspace. Returns
+// cudaErrorNotSupported if tensor maps cannot be made.
 cudaError_t launch_gemm_tc(const void* xperm, const uint8_t* wp, const float* scale, const int* rowsum,
-                           const float* gamma, void* out, bool out_acc, int M, int N, int K, cudaStream_t s);
+                           const float* gamma, void* out, bool out_acc, int M, int N, int K, const TcPlan& plan,
+                           void* sk_ws, cudaStream_t s);
 cudaError_t take_tc_wait_error(int* flag);
 
 }  // namespace bl

@@ -27,8 +27,13 @@
 //     y = fp32(fp32(acc * gamma) / s).
 //
 // Kernel shape: persistent, one CTA per SM, tiles of 128 weight rows x BN
-// tokens (BN chosen per shape from 128..256 so the tiles spread evenly over
-// the SMs), 448 threads:
+// tokens, 448 threads. Whole tiles are dealt round-robin; when the last
+// round would leave most SMs idle, the k-stages of its tiles are instead
+// split evenly over the CTAs ("stream-K"): each CTA adds its partial sum of
+// such a tile into an fp32 buffer with atomic adds, which are exact here
+// (every partial is an integer multiple of 2^-24 below 1 in magnitude), and
+// the CTA whose contribution completes the tile's k-count applies the
+// epilogue from the buffer. The roles:
 //   warp 0      TMA producer: activation tile [BN][64] fp16 (128-byte
 //               swizzle) and packed weight tile [128][16] bytes per stage,
 //               as many stages as fit (5 at BN = 256, 10 at BN = 128: about
@@ -164,11 +169,57 @@ BL_DEVICE float div_rn_markstein(float t, float s, float r) {
 
 }  // namespace
 
+// Work of CTA b (of G): whole tiles b, b + G, ... below dp_tiles, then a run
+// of the k-stages of the split tiles [dp_tiles, dp_tiles + sk_tiles): their
+// sk_tiles * k_iters stages are cut into sk_ctas equal runs, run b for CTA
+// b < sk_ctas. A run is shorter than one tile's stages, so it covers at most
+// the end of one tile and the start of the next.
+struct TcSched {
+  int n_tiles_n;   // tiles along the weight rows
+  int k_iters;     // k-stages per tile
+  int dp_tiles;    // tiles computed whole
+  int sk_tiles;    // tiles split over the CTAs
+  int sk_ctas;     // CTAs that take a run of split-tile stages
+
+  BL_DEVICE void run(int b, long long& u0, long long& u1) const {
+    u0 = u1 = 0;
+    if (b < sk_ctas) {
+      const long long U = static_cast<long long>(sk_tiles) * k_iters;
+      u0 = U * b / sk_ctas;
+      u1 = U * (b + 1) / sk_ctas;
+    }
+  }
+  BL_DEVICE int items(int b, int G) const {
+    const int dp = b < dp_tiles ? (dp_tiles - b + G - 1) / G : 0;
+    long long u0, u1;
+    run(b, u0, u1);
+    return dp + (u1 > u0 ? static_cast<int>((u1 - 1) / k_iters - u0 / k_iters) + 1 : 0);
+  }
+  // item i of CTA b: tile and k-stage range [k0, k1)
+  BL_DEVICE void item(int b, int G, int i, int& tile, int& k0, int& k1) const {
+    const int dp = b < dp_tiles ? (dp_tiles - b + G - 1) / G : 0;
+    if (i < dp) {
+      tile = b + i * G;
+      k0 = 0;
+      k1 = k_iters;
+      return;
+    }
+    long long u0, u1;
+    run(b, u0, u1);
+    const long long t = u0 / k_iters + (i - dp);
+    const long long lo = t * k_iters;
+    k0 = static_cast<int>(u0 > lo ? u0 - lo : 0);
+    k1 = static_cast<int>(u1 - lo < k_iters ? u1 - lo : k_iters);
+    tile = dp_tiles + static_cast<int>(t);
+  }
+};
+
 template <int BN, bool OUT_ACC>
 __global__ void __launch_bounds__(kThreads, 1)
 bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
            const float* __restrict__ scale, const int* __restrict__ rowsum, const float* __restrict__ gamma,
-           void* __restrict__ out, int M, int N, int K) {
+           void* __restrict__ out, int M, int N, int K, TcSched sch, float* __restrict__ sk_buf,
+           int* __restrict__ sk_cnt) {
   constexpr int kStages = stages_for(BN);
   constexpr uint32_t kStageBytes = stage_bytes(BN);
   constexpr uint32_t kXBytes = static_cast<uint32_t>(BN) * kBK * 2;
@@ -183,11 +234,12 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   uint64_t* tfull = efree + kEStages;                            // accumulator b holds a finished tile
   uint64_t* tempty = tfull + 2;                                  // accumulator b has been read out
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  int* s_last = reinterpret_cast<int*>(tmem_slot + 1);         // this CTA completes a split tile
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_tiles_n = (N + kBM - 1) / kBM;
-  const int n_tiles = n_tiles_n * ((M + BN - 1) / BN);
-  const int k_iters = K / kBK;
+  const int n_tiles_n = sch.n_tiles_n;
+  const int n_items = sch.items(blockIdx.x, gridDim.x);
+  (void)K;
   bool ok = true;
 
   if (tid == 0) {
@@ -225,9 +277,11 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // ---- TMA producer
     if (lane == 0) {
       uint32_t g = 0;
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      for (int item = 0; item < n_items; ++item) {
+        int tile, k0, k1;
+        sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
         const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
-        for (int it = 0; it < k_iters; ++it, ++g) {
+        for (int it = k0; it < k1; ++it, ++g) {
           const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
           if (g >= kStages) ok = mbar_wait(&empty[s], ph ^ 1u) && ok;
           uint8_t* st = smem + s * kStageBytes;
@@ -241,12 +295,14 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // ---- MMA issuer
     if (lane == 0) {
       uint32_t g = 0, tcount = 0;
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
+      for (int item = 0; item < n_items; ++item, ++tcount) {
+        int tile, k0, k1;
+        sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
         const uint32_t b = tcount & 1u;
         if (tcount >= 2) ok = mbar_wait(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
         tc_fence_after();
         const uint32_t d = tmem + b * 256u;
-        for (int it = 0; it < k_iters; ++it, ++g) {
+        for (int it = k0; it < k1; ++it, ++g) {
           const uint32_t s = g % kStages, e = g % kEStages, eph = (g / kEStages) & 1u;
           ok = mbar_wait(&expd[e], eph) && ok;   // also means TMA stage s has landed
           tc_fence_after();
@@ -254,7 +310,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16<BN>(d, adesc + 2u * kk, bdesc + 2u * kk, (it | kk) != 0 ? 1u : 0u);
+            umma_f16<BN>(d, adesc + 2u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
           umma_commit(&empty[s]);
           umma_commit(&efree[e]);
         }
@@ -268,8 +324,10 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int r = t & (kBM - 1), h = t >> 7;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     uint32_t g = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-      for (int it = 0; it < k_iters; ++it, ++g) {
+    for (int item = 0; item < n_items; ++item) {
+      int tile, k0, k1;
+      sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
+      for (int it = k0; it < k1; ++it, ++g) {
         const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
         const uint32_t e = g % kEStages, eph = (g / kEStages) & 1u;
         ok = mbar_wait(&full[s], ph) && ok;
@@ -306,7 +364,9 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const float gm = OUT_ACC ? 0.f : __ldg(gamma);
     const bool gamma_fast = OUT_ACC || (gm > 0x1p-72f && gm < 0x1p72f);
     uint32_t tcount = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tcount) {
+    for (int item = 0; item < n_items; ++item, ++tcount) {
+      int tile, k0, k1;
+      sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
       const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
       const uint32_t b = tcount & 1u;
       float* s_scale = reinterpret_cast<float*>(misc + 256 + b * kEpiBytes);
@@ -332,16 +392,13 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const int n = n0 + quarter * 32 + lane;
       float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
       int32_t* arow = OUT_ACC ? static_cast<int32_t*>(out) + static_cast<size_t>(m0) * N + n : nullptr;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + b * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
-        if (n >= N) continue;
+      // y (or acc) of tokens m0 + c0 .. m0 + c0 + 31 of row n from the sums D
+      auto emit = [&](int c0, const float (&dv)[32]) {
         const bool full_chunk = m0 + c0 + 32 <= M;
         if (full_chunk && gamma_fast && s_fast[c0 >> 5]) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float acc = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.f), s_rowsum[c0 + j]);
+            const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
             const size_t o = static_cast<size_t>(c0 + j) * N;
             if constexpr (OUT_ACC) {
               arow[o] = static_cast<int>(acc);
@@ -353,7 +410,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (m0 + c0 + j < M) {
-              const float acc = __fsub_rn(__fmul_rn(__uint_as_float(v[j]), 16777216.f), s_rowsum[c0 + j]);
+              const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
               const size_t o = static_cast<size_t>(c0 + j) * N;
               if constexpr (OUT_ACC) {
                 arow[o] = static_cast<int>(acc);
@@ -368,10 +425,58 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             }
           }
         }
+      };
+      if (tile < sch.dp_tiles) {
+        // a whole tile: straight from TMEM
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + b * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+          if (n >= N) continue;
+          float dv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dv[j] = __uint_as_float(v[j]);
+          emit(c0, dv);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+      } else {
+        // part of a split tile: add the partial into the tile's buffer
+        // [token][row]; the 32 lanes of a warp add 32 consecutive floats
+        const int sk = tile - sch.dp_tiles;
+        float* buf = sk_buf + static_cast<size_t>(sk) * BN * kBM + quarter * 32 + lane;
+        const int m_left = M - m0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + b * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+          if (n >= N) continue;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (c0 + j < m_left) atomicAdd(buf + static_cast<size_t>(c0 + j) * kBM, __uint_as_float(v[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        // the CTA whose stages complete the tile's k-count writes it
+        __threadfence();
+        named_bar(1, 128);
+        if (et == 0) *s_last = atomicAdd(sk_cnt + sk, k1 - k0) + (k1 - k0) == sch.k_iters;
+        named_bar(1, 128);
+        if (*s_last) {
+          __threadfence();
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            if (n >= N) break;
+            float dv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dv[j] = c0 + j < m_left ? __ldcg(buf + static_cast<size_t>(c0 + j) * kBM) : 0.f;
+            emit(c0, dv);
+          }
+        }
+        named_bar(1, 128);                       // s_last is read before the next split tile sets it
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[b]);
     }
   }
 
@@ -468,11 +573,16 @@ template <int XIN>
 __global__ void __launch_bounds__(256)
 bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int M, int K,
             int8_t* __restrict__ xq_out, float* __restrict__ scale_out, __half* __restrict__ xperm,
-            int* __restrict__ rowsum) {
+            int* __restrict__ rowsum, uint4* __restrict__ zero, size_t zero_n16) {
   pdl_wait();
   pdl_launch_dependents();
   x = launder(x);
   scale_in = launder(scale_in);
+  // the contraction's split-tile buffer and counters start from zero (after
+  // the wait: the contraction before this one may still have used them)
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    zero[i] = make_uint4(0u, 0u, 0u, 0u);
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (m >= M) return;
@@ -565,33 +675,55 @@ EncodeTiled encode_fn() {
 
 size_t gemm_tc_smem_bytes() { return smem_for(kMaxBN); }
 
-namespace {
-
-// Token-tile width: the one whose tiles, dealt round-robin to the SMs, finish
-// first. A k-stage costs nearly the same for narrow tiles (the per-stage
-// issue work of the MMA thread, not the tensor pipe, sets its length there),
-// so a tile's time is taken as proportional to max(BN, 200); ties go to the
+// Launch plan: token-tile width BN, grid and work split. For each BN the
+// tiles are dealt round-robin to the SMs; a last round that would occupy at
+// most a tenth of the SMs is split by k-stages instead (stream-K), costed as
+// the fraction of a round it fills plus 5% for the buffer traffic. (Every
+// contributing CTA adds a whole 128 x BN fp32 partial with atomics; with more
+// split tiles that traffic costs more than the idle SMs it saves.)
+// A k-stage costs nearly the same for narrow tiles (the per-stage issue work
+// of the MMA thread, not the tensor pipe, sets its length there), so a
+// tile's time is taken as proportional to max(BN, 200); ties go to the
 // wider tile.
-int pick_bn(int M, int N, int sms) {
+TcPlan tc_plan(int M, int N, int K, int sms) {
   const int cands[5] = {256, 224, 192, 160, 128};
-  int best = 256;
-  long long best_cost = -1;
   const int tn = (N + kBM - 1) / kBM;
+  const int k_iters = K / kBK;
+  TcPlan best;
+  double best_cost = -1.0;
   for (int bn : cands) {
-    const long long tiles = static_cast<long long>(tn) * ((M + bn - 1) / bn);
-    const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * (bn > 200 ? bn : 200);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = bn;
-    }
+    const int tiles = tn * ((M + bn - 1) / bn);
+    const int full = tiles / sms, r = tiles % sms;
+    const bool sk = r > 0 && 10 * r <= sms;
+    const double rounds = r == 0 ? full : (sk ? full + static_cast<double>(r) / sms + 0.05 : full + 1.0);
+    const double cost = rounds * (bn > 200 ? bn : 200);
+    if (best_cost >= 0.0 && cost >= best_cost) continue;
+    best_cost = cost;
+    TcPlan p;
+    p.bn = bn;
+    p.n_tiles_n = tn;
+    p.k_iters = k_iters;
+    p.dp_tiles = sk ? full * sms : tiles;
+    p.sk_tiles = sk ? r : 0;
+    long long ctas = sk ? static_cast<long long>(r) * k_iters / 4 : 0;   // runs of at least 4 stages
+    if (ctas > sms) ctas = sms;
+    if (sk && ctas < 1) ctas = 1;
+    p.sk_ctas = static_cast<int>(ctas);
+    p.grid = full > 0 ? sms : (sk ? p.sk_ctas : tiles);
+    const size_t buf = static_cast<size_t>(p.sk_tiles) * bn * kBM * 4;
+    p.sk_buf_bytes = (buf + 255) / 256 * 256;
+    p.sk_bytes = p.sk_buf_bytes + (static_cast<size_t>(p.sk_tiles) * 4 + 255) / 256 * 256;
+    best = p;
   }
   return best;
 }
 
+namespace {
+
 template <int BN, bool OUT_ACC>
 cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale, const int* rowsum,
-                        const float* gamma, void* out, int M, int N, int K, int sms, cudaStream_t s) {
+                        const float* gamma, void* out, int M, int N, int K, const TcPlan& p, void* sk_ws,
+                        cudaStream_t s) {
   static size_t done = 0;
   constexpr size_t smem = smem_for(BN);
   static_assert(smem <= kSmemBudget, "shared memory budget");
@@ -602,48 +734,56 @@ cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
     if (e != cudaSuccess) return e;
     done = smem;
   }
-  const int tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
-  const int grid = tiles < sms ? tiles : sms;
-  return launch_pdl(bl_gemm_tc<BN, OUT_ACC>, dim3(grid), dim3(kThreads), smem, s, tm_x, tm_w, scale, rowsum, gamma,
-                    out, M, N, K);
+  TcSched sch;
+  sch.n_tiles_n = p.n_tiles_n;
+  sch.k_iters = p.k_iters;
+  sch.dp_tiles = p.dp_tiles;
+  sch.sk_tiles = p.sk_tiles;
+  sch.sk_ctas = p.sk_ctas;
+  float* sk_buf = static_cast<float*>(sk_ws);
+  int* sk_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(sk_ws) + p.sk_buf_bytes);
+  return launch_pdl(bl_gemm_tc<BN, OUT_ACC>, dim3(p.grid), dim3(kThreads), smem, s, tm_x, tm_w, scale, rowsum, gamma,
+                    out, M, N, K, sch, sk_buf, sk_cnt);
 }
 
 template <bool OUT_ACC>
-cudaError_t launch_tc_bn(int bn, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale,
-                         const int* rowsum, const float* gamma, void* out, int M, int N, int K, int sms,
+cudaError_t launch_tc_bn(const TcPlan& p, const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale,
+                         const int* rowsum, const float* gamma, void* out, int M, int N, int K, void* sk_ws,
                          cudaStream_t s) {
-  switch (bn) {
-    case 224: return launch_tc_t<224, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
-    case 192: return launch_tc_t<192, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
-    case 160: return launch_tc_t<160, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
-    case 128: return launch_tc_t<128, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
-    default: return launch_tc_t<256, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+  switch (p.bn) {
+    case 224: return launch_tc_t<224, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
+    case 192: return launch_tc_t<192, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
+    case 160: return launch_tc_t<160, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
+    case 128: return launch_tc_t<128, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
+    default: return launch_tc_t<256, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M, int K, int8_t* xq_out,
-                            float* scale_out, void* xperm, int* rowsum, cudaStream_t s) {
+                            float* scale_out, void* xperm, int* rowsum, void* zero, size_t zero_bytes,
+                            cudaStream_t s) {
   __half* xp = static_cast<__half*>(xperm);
+  uint4* z = static_cast<uint4*>(zero);
+  const size_t n16 = zero_bytes / 16;
   const int grid = (M + 7) / 8;
   if (xin == kXinF32)
     return launch_pdl(bl_act_perm<kXinF32>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
-                      rowsum);
+                      rowsum, z, n16);
   if (xin == kXinBF16)
     return launch_pdl(bl_act_perm<kXinBF16>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
-                      rowsum);
-  return launch_pdl(bl_act_perm<kXinI8>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp, rowsum);
+                      rowsum, z, n16);
+  return launch_pdl(bl_act_perm<kXinI8>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp, rowsum,
+                    z, n16);
 }
 
 cudaError_t launch_gemm_tc(const void* xperm, const uint8_t* wp, const float* scale, const int* rowsum,
-                           const float* gamma, void* out, bool out_acc, int M, int N, int K, cudaStream_t s) {
+                           const float* gamma, void* out, bool out_acc, int M, int N, int K, const TcPlan& plan,
+                           void* sk_ws, cudaStream_t s) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (sms <= 0) sms = 148;
-  const int bn = pick_bn(M, N, sms);
+  const int bn = plan.bn;
   CUtensorMap tm_x, tm_w;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
@@ -665,8 +805,8 @@ cudaError_t launch_gemm_tc(const void* xperm, const uint8_t* wp, const float* sc
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  if (out_acc) return launch_tc_bn<true>(bn, tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
-  return launch_tc_bn<false>(bn, tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sms, s);
+  if (out_acc) return launch_tc_bn<true>(plan, tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sk_ws, s);
+  return launch_tc_bn<false>(plan, tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, sk_ws, s);
 }
 
 cudaError_t take_tc_wait_error(int* flag) {

@@ -80,6 +80,17 @@ def test_shapes(m, n, k, xdt):
     compare_full(w, x)
 
 
+@pytest.mark.parametrize("m,n,k", [(100, 300, 1024), (700, 500, 2048), (512, 896, 4096), (512, 19200, 256)])
+def test_split_tile_contraction(m, n, k):
+    """Tensor-core shapes whose tiles are split by k-stages over several CTAs
+    (partial sums meet in the fp32 buffer): a few tiles with ragged M and N,
+    runs that cross tile boundaries, and whole tiles followed by a split
+    remainder."""
+    w = gaussian_weights(n, k, seed=3000 + n + k)
+    x = gaussian_activations(m, k, seed=4000 + m + k)
+    compare_full(w, x)
+
+
 # ------------------------------------------------------------------ degenerate and special values
 def test_zero_token_and_zero_weights():
     w = gaussian_weights(64, 256, seed=5)
