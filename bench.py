@@ -376,6 +376,20 @@ def max_over_ranks(v, world, device):
     return float(t.item())
 
 
+STEP_DESC = ("pack_weights (absmean, codes, packing) + forward (act quant, contraction, rescale) per projection")
+
+
+def base_config(wl, world):
+    """The config fields both arms report for a workload."""
+    return {"workload": wl.name, "description": wl.description,
+            "projections": [f"{p.name}: M={p.m} K={p.k} N={p.n}"
+                            for p in wl.projections[:len(wl.projections) // max(wl.layers, 1)]],
+            "layers": wl.layers,
+            "step": STEP_DESC if wl.layers == 1 else "forward (act quant, contraction, rescale) of every projection; "
+                                                      "weights packed once at set-up",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
@@ -389,7 +403,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r["seconds"] / r["steps"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f32",
             "data": "synthetic (seeded generators)",
-            "config": {"workload": wl.name, "description": wl.description},
+            "config": base_config(wl, world),
             "cpu_baseline": {"value": r["value"], "unit": unit, "cores": r["cores"], "kind": "oracle",
                              "sample": r["sample"]},
             "e2e": {"value": r["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -541,14 +555,11 @@ def main(argv=None):
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8/i8/i32 (f32 scales)", "data": "synthetic (seeded generators)",
-        "config": {"workload": wl.name, "description": wl.description,
-                   "projections": [f"{p.name}: M={p.m} K={p.k} N={p.n}" for p in projs],
-                   "step": "pack_weights (absmean, codes, packing) + forward (act quant, contraction, "
-                           "rescale) per projection",
+        "config": {**base_config(wl, world),
                    "units_per_step": units_step,
                    "l2": f"inputs larger than L2: {args.rotate} rotating input sets of "
                          f"{sum(4 * p.n * p.k + 2 * p.m * p.k for p in projs) / 1e6:.1f} MB",
-                   "graph_steps": G, "parallelism": f"replicas x{world}",
+                   "graph_steps": G,
                    "rows_timing": "rows and roofline from a second timed pass whose graph has event nodes "
                                   "between the calls (each call alone, no overlap with its neighbours)"},
         "roofline": roof,
