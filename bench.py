@@ -70,7 +70,7 @@ def row_kernels(p):
     if p.k % 64 == 0 and p.m >= 65:
         fwd = ["bl_act_perm", "bl_gemm_tc"]
     elif p.k % 64 == 0 and p.m <= 4:
-        fwd = ["bl_gemv_fused"]
+        fwd = ["bl_act_tq", "bl_gemv_w"]
     elif p.k % 64 == 0 and p.m <= FUSED_MAX_M:
         fwd = ["bl_decode_mma"]
     else:

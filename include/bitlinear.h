@@ -171,10 +171,17 @@ BL_API bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int6
  *            also written there.
  * scale_out  optional fp32 [M]: if non-NULL the per-token scales are written.
  * workspace  at least bitlinear_forward_workspace_bytes(M, N, K) bytes,
- *            256-byte aligned (may be NULL when that size is 0).
+ *            256-byte aligned (may be NULL when that size is 0). Scratch:
+ *            its contents need no initialisation and are overwritten. The
+ *            size depends on the current device's SM count (the tensor-core
+ *            path keeps a split-tile buffer there), so query it on the device
+ *            that runs the call.
  *
- * The kernel is chosen by M: a dp4a GEMV for M <= 4, tcgen05 tensor-core
- * kernels otherwise.
+ * The kernels are chosen by M and K: with K % 64 == 0, a dp4a GEMV with the
+ * activation pass ahead of it for M <= 4, a fused mma.sync kernel for
+ * M <= 8, activation quantisation plus mma.sync for M <= 64, and the tcgen05
+ * tensor-core path for M >= 65; K % 64 != 0 takes the activation pass plus a
+ * dp4a kernel. Calls that share a workspace must not overlap on the GPU.
  * ------------------------------------------------------------------------- */
 BL_API size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
