@@ -56,6 +56,28 @@ BL_DEVICE bool mbar_wait(uint64_t* bar, uint32_t phase) {
   return false;
 }
 
+// One wait that may suspend the thread for up to kSleepNs before it gives up
+// (it resumes as soon as the phase completes), for consumers that would
+// otherwise poll for a long time while a copy is in flight.
+constexpr uint32_t kSleepNs = 20000;
+constexpr uint32_t kSleepTries = 1u << 14;   // a wait gives up after at most ~0.33 s
+BL_DEVICE bool mbar_try_sleep(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase), "n"(kSleepNs)
+      : "memory");
+  return ok != 0u;
+}
+BL_DEVICE bool mbar_wait_sleep(uint64_t* bar, uint32_t phase) {
+  for (uint32_t i = 0; i < kSleepTries; ++i)
+    if (mbar_try_sleep(bar, phase)) return true;
+  return false;
+}
+
 // Global -> shared bulk copy completing on an mbarrier (both addresses 16-byte
 // aligned, bytes a multiple of 16).
 BL_DEVICE void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -31,10 +31,10 @@ bl_status record_error(bl_status st, const char* msg);
 // ---- weight packing (pack.cu)
 // Both weight-pass kernels stream W through a ring of shared-memory stages
 // filled by bulk copies: consumer threads plus one producer warp.
-constexpr int kAbsumThreads = 512;          // consumers of the exact-sum kernel
+constexpr int kAbsumThreads = 256;          // consumers of the exact-sum kernel
 constexpr int kPackThreads = 256;           // consumers of the packing kernel
 constexpr int kRingStageF4 = 1024;          // float4 per stage (16 KB)
-constexpr int kRingStages = 6;              // stages in flight per CTA
+constexpr int kRingStages = 4;              // stages in flight per CTA (64 KB)
 constexpr uint32_t kRingSmem = kRingStages * kRingStageF4 * 16;
 // Bytes of W the exact-sum pass marks to stay in L2 for the packing pass
 // (three quarters of a 126 MB L2).

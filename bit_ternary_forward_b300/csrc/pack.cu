@@ -178,7 +178,7 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
     for (int j = 0; j < n_stages; ++j) {
       const int s = j % kRingStages;
       // warp-uniform verdict, so a timed-out lane cannot split the warp
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (j / kRingStages) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&s_full[s], (j / kRingStages) & 1))) {
         ok = false;
         break;
       }
@@ -451,7 +451,7 @@ bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __re
     const int rot = (tid >> 1) & 3;
     for (int j = 0; j < n_stages; ++j) {
       const int s = j % kRingStages;
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (j / kRingStages) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(&s_full[s], (j / kRingStages) & 1))) {
         ok = false;
         break;
       }
