@@ -163,6 +163,15 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- ncu traffic record
+def source_hash(src):
+    """sha256 (16 hex digits) of a kernel source and the headers every kernel includes."""
+    h = hashlib.sha256()
+    for name in (src, "kernels.cuh", "common.cuh", "async.cuh"):
+        with open(os.path.join(ROOT, "bit_ternary_forward_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel_row, prefill=False):
     """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -171,8 +180,7 @@ def traffic_record(kernel_row, prefill=False):
     src = {"pack_weights": "pack.cu", "forward": "gemv_fused.cu"}[kernel_row]
     if kernel_row == "forward" and prefill:
         src = "prefill.cu"
-    with open(os.path.join(ROOT, "bit_ternary_forward_b300", "csrc", src), "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = source_hash(src)
     best = None
     for line in open(path):
         parts = line.split()
