@@ -106,7 +106,8 @@ cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const f
 cudaError_t take_gemv_wait_error(int* flag);
 
 // ---- prefill contraction on tcgen05 (prefill.cu)
-constexpr int kTcMinM = 65;   // smallest M routed to the tensor-core kernel
+constexpr int kTcMinM = 17;   // smallest M routed to the tensor-core kernel (below it the
+                              // mma.sync decode kernel is faster on B300)
 size_t gemm_tc_smem_bytes();
 // Launch plan of the tensor-core contraction (tc_plan, prefill.cu): token-tile
 // width, grid, whole tiles and split ("stream-K") tiles, and the bytes of its

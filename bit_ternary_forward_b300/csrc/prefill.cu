@@ -680,25 +680,31 @@ size_t gemm_tc_smem_bytes() { return smem_for(kMaxBN); }
 // most a tenth of the SMs is split by k-stages instead (stream-K), costed as
 // the fraction of a round it fills plus 5% for the buffer traffic. (Every
 // contributing CTA adds a whole 128 x BN fp32 partial with atomics; with more
-// split tiles that traffic costs more than the idle SMs it saves.)
+// split tiles that traffic costs more than the idle SMs it saves.) A narrow
+// tile that holds every token (M <= BN <= 64) has small partials, so when
+// there are fewer such tiles than SMs they are always split.
 // A k-stage costs nearly the same for narrow tiles (the per-stage issue work
 // of the MMA thread, not the tensor pipe, sets its length there), so a
-// tile's time is taken as proportional to max(BN, 200); ties go to the
-// wider tile.
+// tile's time is taken as proportional to max(BN, 200); among equal costs the
+// plan with fewer token tiles, then the narrower tile, wins (a narrower stage
+// leaves room for more of them in shared memory).
 TcPlan tc_plan(int M, int N, int K, int sms) {
-  const int cands[5] = {256, 224, 192, 160, 128};
+  const int cands[7] = {256, 224, 192, 160, 128, 64, 32};
   const int tn = (N + kBM - 1) / kBM;
   const int k_iters = K / kBK;
   TcPlan best;
   double best_cost = -1.0;
+  int best_tm = 0;
   for (int bn : cands) {
-    const int tiles = tn * ((M + bn - 1) / bn);
+    const int tm = (M + bn - 1) / bn;
+    const int tiles = tn * tm;
     const int full = tiles / sms, r = tiles % sms;
-    const bool sk = r > 0 && 10 * r <= sms;
+    const bool sk = r > 0 && (10 * r <= sms || (full == 0 && bn <= 64 && tm == 1));
     const double rounds = r == 0 ? full : (sk ? full + static_cast<double>(r) / sms + 0.05 : full + 1.0);
     const double cost = rounds * (bn > 200 ? bn : 200);
-    if (best_cost >= 0.0 && cost >= best_cost) continue;
+    if (best_cost >= 0.0 && (cost > best_cost || (cost == best_cost && tm > best_tm))) continue;
     best_cost = cost;
+    best_tm = tm;
     TcPlan p;
     p.bn = bn;
     p.n_tiles_n = tn;
@@ -755,6 +761,8 @@ cudaError_t launch_tc_bn(const TcPlan& p, const CUtensorMap& tm_x, const CUtenso
     case 192: return launch_tc_t<192, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
     case 160: return launch_tc_t<160, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
     case 128: return launch_tc_t<128, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
+    case 64: return launch_tc_t<64, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
+    case 32: return launch_tc_t<32, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
     default: return launch_tc_t<256, OUT_ACC>(tm_x, tm_w, scale, rowsum, gamma, out, M, N, K, p, sk_ws, s);
   }
 }
