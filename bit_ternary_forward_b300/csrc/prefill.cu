@@ -48,7 +48,9 @@
 //               accumulator: tcgen05.ld 32x32b (TMEM lane = weight row, one
 //               lane quarter per warp), stores coalesced along the rows.
 // Every wait on the full / expanded / empty stage barriers and on the
-// accumulator barriers is bounded.
+// accumulator barriers is bounded, and sleeps until its phase completes
+// instead of polling: polling warps take issue slots from the MMA thread
+// (measured 4-6 % slower).
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -283,7 +285,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
         for (int it = k0; it < k1; ++it, ++g) {
           const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
-          if (g >= kStages) ok = mbar_wait(&empty[s], ph ^ 1u) && ok;
+          if (g >= kStages) ok = mbar_wait_sleep(&empty[s], ph ^ 1u) && ok;
           uint8_t* st = smem + s * kStageBytes;
           mbar_expect_tx(&full[s], kXBytes + kWpBytes);
           tma_load_2d(st, &tm_x, it * kBK, m0, &full[s]);
@@ -299,12 +301,12 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         int tile, k0, k1;
         sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
         const uint32_t b = tcount & 1u;
-        if (tcount >= 2) ok = mbar_wait(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
+        if (tcount >= 2) ok = mbar_wait_sleep(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
         tc_fence_after();
         const uint32_t d = tmem + b * 256u;
         for (int it = k0; it < k1; ++it, ++g) {
           const uint32_t s = g % kStages, e = g % kEStages, eph = (g / kEStages) & 1u;
-          ok = mbar_wait(&expd[e], eph) && ok;   // also means TMA stage s has landed
+          ok = mbar_wait_sleep(&expd[e], eph) && ok;   // also means TMA stage s has landed
           tc_fence_after();
           const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes));   // activations [BN][64]
           const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
@@ -330,8 +332,8 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       for (int it = k0; it < k1; ++it, ++g) {
         const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
         const uint32_t e = g % kEStages, eph = (g / kEStages) & 1u;
-        ok = mbar_wait(&full[s], ph) && ok;
-        if (g >= kEStages) ok = mbar_wait(&efree[e], eph ^ 1u) && ok;
+        ok = mbar_wait_sleep(&full[s], ph) && ok;
+        if (g >= kEStages) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
         const uint2 pw = *reinterpret_cast<const uint2*>(smem + s * kStageBytes + kXBytes + r * 16 + h * 8);
         uint8_t* row = we_base + e * kWeBytes + r * 128;
         const uint32_t words[2] = {pw.x, pw.y};
@@ -387,7 +389,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (lane == 0) s_fast[c] = all == 0xffffffffu;
       }
       named_bar(1, 128);                         // the per-token data is complete
-      ok = mbar_wait(&tfull[b], (tcount >> 1) & 1u) && ok;
+      ok = mbar_wait_sleep(&tfull[b], (tcount >> 1) & 1u) && ok;
       tc_fence_after();
       const int n = n0 + quarter * 32 + lane;
       float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
