@@ -67,7 +67,7 @@ FUSED_MAX_M = 8     # the forward quantises activations inside the contraction u
 
 
 def row_kernels(p):
-    if p.k % 64 == 0 and p.m >= 65:
+    if p.k % 64 == 0 and p.m >= 17:
         fwd = ["bl_act_perm", "bl_gemm_tc"]
     elif p.k % 64 == 0 and p.m <= 4:
         fwd = ["bl_act_tq", "bl_gemv_w"]
@@ -172,8 +172,8 @@ def source_hash(src):
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel_row, prefill=False):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+def traffic_record(kernel_row, workload, prefill=False):
+    """DRAM bytes per launch from the committed ncu summary of this workload, if the kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -184,7 +184,7 @@ def traffic_record(kernel_row, prefill=False):
     best = None
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == kernel_row and parts[2] == h:
+        if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == kernel_row and parts[2] == h and parts[3] == workload:
             best = float(parts[4])
     return best
 
@@ -540,11 +540,12 @@ def main(argv=None):
     dom = max(rows, key=lambda e: e["share"])
     if unit == "GB/s" or dom["row"] != "forward":
         roof = {"bound": "hbm", "achieved": dom["gbs"], "peak": hbm, "unit": "GB/s", "frac": dom["gbs"] / hbm,
-                "traffic": traffic_record(dom["row"], unit != "GB/s"), "kernel": dom["row"] + " (" + "+".join(dom["kernels"]) + ")",
+                "traffic": traffic_record(dom["row"], wl.name, unit != "GB/s"),
+                "kernel": dom["row"] + " (" + "+".join(dom["kernels"]) + ")",
                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
     else:
         roof = {"bound": "tensor", "achieved": dom["tops"], "peak": bf16, "unit": "TFLOP/s",
-                "frac": dom["tops"] / bf16, "traffic": traffic_record(dom["row"], True),
+                "frac": dom["tops"] / bf16, "traffic": traffic_record(dom["row"], wl.name, True),
                 "kernel": dom["row"] + " (" + "+".join(dom["kernels"]) + "; fp16 tcgen05.mma, exact)",
                 "peak_source": f"MEASURED_PEAKS.json bf16_tflops burst ({peak_src}); fp16 runs at the bf16 rate",
                 "frac_of_sustained": dom["tops"] / bf16_sus}

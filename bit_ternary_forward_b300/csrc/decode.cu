@@ -270,7 +270,7 @@ bl_decode_mma(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
     for (int tl0 = 0; tl0 < n_tiles; tl0 += 6) {
       const int nt = min(6, n_tiles - tl0);
       if (m0 == 0) {
-        for (int i = 0; i < nt; ++i) ok = mbar_wait(&s_bar[tl0 + i], 0u) && ok;
+        for (int i = 0; i < nt; ++i) ok = mbar_wait_sleep(&s_bar[tl0 + i], 0u) && ok;
       }
       for (int ks = warp; ks < ksteps; ks += kWarps) {
         const uint2 bv = *reinterpret_cast<const uint2*>(xrow + 32 * ks);
