@@ -22,3 +22,9 @@ from .bitlinear_oracle import (  # noqa: F401
     ternary_int8_matmul,
     unpack_codes,
 )
+from .quantizer_variants import (  # noqa: F401,E402
+    DEFAULT_FACTOR,
+    alpha_round_quantize,
+    scaled_mean,
+    threshold_quantize,
+)
