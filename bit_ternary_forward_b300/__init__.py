@@ -25,6 +25,8 @@ LIB_PATH = os.path.join(_HERE, "libbitlinear.so")
 
 BL_OK, BL_ERR_INVALID_ARG, BL_ERR_UNSUPPORTED, BL_ERR_CUDA, BL_ERR_WORKSPACE = range(5)
 BL_F32, BL_BF16 = 0, 1
+#: weight quantisers of bitlinear_pack_weights_quantizer (bl_quantizer)
+QUANTIZERS = {"absmean": 0, "alpha_round": 1, "threshold": 2}
 
 
 class BitLinearError(RuntimeError):
@@ -43,6 +45,7 @@ def _load() -> ctypes.CDLL:
         "bitlinear_pack_workspace_bytes": (sz, [i64, i64]),
         "bitlinear_pack_weights": (st, [vp, i64, i64, vp, vp, vp, sz, vp]),
         "bitlinear_pack_weights_noalloc": (st, [vp, i64, i64, vp, vp, vp]),
+        "bitlinear_pack_weights_quantizer": (st, [vp, i64, i64, ctypes.c_int, ctypes.c_float, vp, vp, vp, sz, vp]),
         "bitlinear_absmean": (st, [vp, i64, i64, vp, vp, sz, vp]),
         "bitlinear_quantize_pack": (st, [vp, i64, i64, vp, vp, vp]),
         "bitlinear_gemm_workspace_bytes": (sz, [i64, i64, i64]),
@@ -119,19 +122,33 @@ def forward_workspace_bytes(m: int, n: int, k: int) -> int:
 
 
 def pack_weights(w: torch.Tensor, out: Optional[PackedWeight] = None,
-                 workspace: Optional[torch.Tensor] = None) -> PackedWeight:
-    """Absmean ternary quantisation and 2-bit packing of fp32 weights [N][K]."""
+                 workspace: Optional[torch.Tensor] = None, quantizer: str = "absmean",
+                 factor: float = 0.7) -> PackedWeight:
+    """Ternary quantisation and 2-bit packing of fp32 weights [N][K].
+
+    quantizer: "absmean" (the default rule; factor unused), "alpha_round" or
+    "threshold" (bitlinear_pack_weights_quantizer); the returned scale (the
+    PackedWeight's gamma) is what the forward multiplies by.
+    """
     _cuda(w, "W", torch.float32)
     if w.dim() != 2:
         raise ValueError("W must be 2-D [N][K]")
+    if quantizer not in QUANTIZERS:
+        raise ValueError(f"unknown quantizer {quantizer!r}; expected one of {sorted(QUANTIZERS)}")
     n, k = w.shape
     if out is None:
         out = PackedWeight(torch.empty((n, k // 4), dtype=torch.uint8, device=w.device),
                            torch.empty(1, dtype=torch.float32, device=w.device), n, k)
     hold, ws, wsn = _workspace(pack_workspace_bytes(n, k), w.device, workspace)
-    _check("bitlinear_pack_weights",
-           lib.bitlinear_pack_weights(w.data_ptr(), n, k, out.wp.data_ptr(), out.gamma.data_ptr(),
-                                      ws, wsn, _stream(w.device)))
+    if quantizer == "absmean":
+        _check("bitlinear_pack_weights",
+               lib.bitlinear_pack_weights(w.data_ptr(), n, k, out.wp.data_ptr(), out.gamma.data_ptr(),
+                                          ws, wsn, _stream(w.device)))
+    else:
+        _check("bitlinear_pack_weights_quantizer",
+               lib.bitlinear_pack_weights_quantizer(w.data_ptr(), n, k, QUANTIZERS[quantizer], float(factor),
+                                                    out.wp.data_ptr(), out.gamma.data_ptr(), ws, wsn,
+                                                    _stream(w.device)))
     return out
 
 

@@ -230,17 +230,6 @@ bl_status check_pack_args(const float* W, int64_t N, int64_t K, const void* Wp_o
   return BL_OK;
 }
 
-// Resident CTAs per SM of a ring kernel with kRingSmem bytes of dynamic shared
-// memory and `threads` threads (0 when the shared memory cannot be reserved).
-int ring_ctas_per_sm(const void* kern, int threads) {
-  int n = 0;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bl::kRingSmem)) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, bl::kRingSmem) != cudaSuccess)
-    n = 0;
-  return n;
-}
-
 // One wave of ring CTAs, each with at least one stage of work.
 uint64_t ring_grid(uint64_t stages, int per_sm) {
   const uint64_t wave = static_cast<uint64_t>(sm_count()) * static_cast<uint64_t>(per_sm);
@@ -248,39 +237,63 @@ uint64_t ring_grid(uint64_t stages, int per_sm) {
   return g < 1 ? 1 : g;
 }
 
-// Exact-sum partials of |W| into `partials`; returns their count in *n_partials.
-bl_status run_absum(const float* W, int64_t N, int64_t K, uint32_t* partials, int* n_partials, cudaStream_t s) {
-  static const int per_sm = ring_ctas_per_sm(reinterpret_cast<const void*>(bl::bl_absum_partials), bl::kAbsumThreads + 32);
+// Exact-sum partials of |W| into `partials`; returns their count in
+// *n_partials. With mask_gamma, only |w| > fp32(factor x *mask_gamma) count.
+bl_status run_absum(const float* W, int64_t N, int64_t K, uint32_t* partials, int* n_partials,
+                    const float* mask_gamma, float factor, cudaStream_t s) {
+  const int per_sm = bl::absum_ctas_per_sm(mask_gamma != nullptr);
   if (per_sm <= 0) return fail(BL_ERR_CUDA, "bl_absum_partials: cannot reserve %u bytes of shared memory", bl::kRingSmem);
   const uint64_t n4 = static_cast<uint64_t>(N) * static_cast<uint64_t>(K) / 4;
   uint64_t ga = ring_grid((n4 + bl::kRingStageF4 - 1) / bl::kRingStageF4, per_sm);
   if (ga > static_cast<uint64_t>(bl::kMaxAbsumCtas)) ga = bl::kMaxAbsumCtas;
-  cudaError_t e = bl::launch_pdl(bl::bl_absum_partials, dim3(static_cast<unsigned>(ga)), dim3(bl::kAbsumThreads + 32),
-                                 bl::kRingSmem, s, reinterpret_cast<const float4*>(W), n4, partials);
+  cudaError_t e = bl::launch_absum(reinterpret_cast<const float4*>(W), n4, partials, mask_gamma, factor,
+                                   static_cast<unsigned>(ga), s);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_absum_partials: %s", cudaGetErrorString(e));
   *n_partials = static_cast<int>(ga);
+  return BL_OK;
+}
+
+bl_status run_finalize(const uint32_t* partials, int n_partials, int64_t N, int64_t K, float* out, cudaStream_t s) {
+  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
+  cudaError_t e = bl::launch_pdl(bl::bl_gamma_finalize, dim3(1), dim3(256), 0, s, partials, n_partials, nk, out);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gamma_finalize: %s", cudaGetErrorString(e));
   return BL_OK;
 }
 
 bl_status run_absmean(const float* W, int64_t N, int64_t K, float* gamma, void* workspace, cudaStream_t s) {
   uint32_t* partials = static_cast<uint32_t*>(workspace);
   int n_partials = 0;
-  if (bl_status st = run_absum(W, N, K, partials, &n_partials, s)) return st;
-  const uint64_t nk = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
-  cudaError_t e = bl::launch_pdl(bl::bl_gamma_finalize, dim3(1), dim3(256), 0, s, static_cast<const uint32_t*>(partials),
-                                 n_partials, nk, gamma);
-  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gamma_finalize: %s", cudaGetErrorString(e));
+  if (bl_status st = run_absum(W, N, K, partials, &n_partials, nullptr, 0.f, s)) return st;
+  return run_finalize(partials, n_partials, N, K, gamma, s);
+}
+
+// Codes and packing (see launch_quant_pack).
+bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma_in, const uint32_t* partials,
+                            int n_partials, float* scale_out, uint8_t* Wp, int rule, float factor, cudaStream_t s) {
+  const uint64_t n_bytes = static_cast<uint64_t>(N) * static_cast<uint64_t>(K) / 4;
+  cudaError_t e = bl::launch_quant_pack(reinterpret_cast<const float4*>(W), n_bytes, gamma_in, partials, n_partials,
+                                        scale_out, reinterpret_cast<uint32_t*>(Wp), rule, factor, sm_count(), s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_quant_pack: %s", cudaGetErrorString(e));
   return BL_OK;
 }
 
-// Codes and packing (see launch_quant_pack for the fused form).
-bl_status run_quantize_pack(const float* W, int64_t N, int64_t K, float* gamma, const uint32_t* partials,
-                            int n_partials, uint8_t* Wp, cudaStream_t s) {
-  const uint64_t n_bytes = static_cast<uint64_t>(N) * static_cast<uint64_t>(K) / 4;
-  cudaError_t e = bl::launch_quant_pack(reinterpret_cast<const float4*>(W), n_bytes, gamma, partials, n_partials,
-                                        reinterpret_cast<uint32_t*>(Wp), sm_count(), s);
-  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_quant_pack: %s", cudaGetErrorString(e));
-  return BL_OK;
+// The whole packing by one rule. absmean and alpha-round: the exact sum, then
+// the packing pass, which combines gamma itself and writes the scale. The
+// threshold rule: gamma into *scale, the masked exact sum (reading gamma
+// there), the packing pass (reading it too), and last the masked mean into
+// *scale; each kernel reads gamma only after its dependency wait, so the
+// final write cannot overtake a read.
+bl_status run_pack(const float* W, int64_t N, int64_t K, int rule, float factor, uint8_t* Wp, float* scale,
+                   void* workspace, cudaStream_t s) {
+  uint32_t* partials = static_cast<uint32_t*>(workspace);
+  int n_partials = 0;
+  if (bl_status st = run_absum(W, N, K, partials, &n_partials, nullptr, 0.f, s)) return st;
+  if (rule != bl::kRuleThreshold)
+    return run_quantize_pack(W, N, K, nullptr, partials, n_partials, scale, Wp, rule, factor, s);
+  if (bl_status st = run_finalize(partials, n_partials, N, K, scale, s)) return st;
+  if (bl_status st = run_absum(W, N, K, partials, &n_partials, scale, factor, s)) return st;
+  if (bl_status st = run_quantize_pack(W, N, K, scale, nullptr, 0, nullptr, Wp, rule, factor, s)) return st;
+  return run_finalize(partials, n_partials, N, K, scale, s);
 }
 
 bl_status check_pack_workspace(int64_t N, int64_t K, const void* workspace, size_t ws_bytes) {
@@ -305,7 +318,8 @@ bl_status bitlinear_quantize_pack(const float* W, int64_t N, int64_t K, const fl
   g_last_error.clear();
   if (bl_status st = check_pack_args(W, N, K, Wp, gamma)) return st;
   if (!Wp) return fail(BL_ERR_INVALID_ARG, "null pointer (Wp)");
-  return run_quantize_pack(W, N, K, const_cast<float*>(gamma), nullptr, 0, Wp, reinterpret_cast<cudaStream_t>(stream));
+  return run_quantize_pack(W, N, K, gamma, nullptr, 0, nullptr, Wp, bl::kRuleAbsmean, 0.f,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, uint8_t* Wp, float* gamma,
@@ -317,10 +331,26 @@ bl_status bitlinear_pack_weights(const float* W, int64_t N, int64_t K, uint8_t* 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // gamma is combined inside the packing kernel, which starts streaming W
   // while the exact sum finishes
-  uint32_t* partials = static_cast<uint32_t*>(workspace);
-  int n_partials = 0;
-  if (bl_status st = run_absum(W, N, K, partials, &n_partials, s)) return st;
-  return run_quantize_pack(W, N, K, gamma, partials, n_partials, Wp, s);
+  return run_pack(W, N, K, bl::kRuleAbsmean, 0.f, Wp, gamma, workspace, s);
+}
+
+bl_status bitlinear_pack_weights_quantizer(const float* W, int64_t N, int64_t K, bl_quantizer quantizer, float factor,
+                                           uint8_t* Wp, float* scale, void* workspace, size_t ws_bytes,
+                                           bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_pack_args(W, N, K, Wp, scale)) return st;
+  if (!Wp) return fail(BL_ERR_INVALID_ARG, "null pointer (Wp)");
+  int rule = bl::kRuleAbsmean;
+  switch (quantizer) {
+    case BL_QUANT_ABSMEAN: rule = bl::kRuleAbsmean; break;
+    case BL_QUANT_ALPHA_ROUND: rule = bl::kRuleAlphaRound; break;
+    case BL_QUANT_THRESHOLD: rule = bl::kRuleThreshold; break;
+    default: return fail(BL_ERR_INVALID_ARG, "unknown quantizer %d", static_cast<int>(quantizer));
+  }
+  if (rule != bl::kRuleAbsmean && !(factor > 0.f && factor < 3.4e38f))
+    return fail(BL_ERR_INVALID_ARG, "factor must be positive and finite (got %g)", static_cast<double>(factor));
+  if (bl_status st = check_pack_workspace(N, K, workspace, ws_bytes)) return st;
+  return run_pack(W, N, K, rule, factor, Wp, scale, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K, int8_t* xq, float* scale,

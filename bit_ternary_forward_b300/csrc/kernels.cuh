@@ -42,15 +42,26 @@ constexpr uint64_t kL2KeepBytes = 96ull << 20;
 constexpr int kPartialWords = 16;          // one 64-byte exact partial per CTA (12 limbs used)
 constexpr int kMaxAbsumCtas = 1184;        // 8 per SM on 148 SMs
 
-__global__ void bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials);
+// Rules of the packing pass (how gamma becomes the code threshold and scale).
+constexpr int kRuleAbsmean = 0;      // codes of W / (gamma + 1e-5), scale gamma
+constexpr int kRuleAlphaRound = 1;   // codes of W / alpha, alpha = fp32(factor x gamma), scale alpha
+constexpr int kRuleThreshold = 2;    // codes sign(W) [|W| > fp32(factor x gamma)], scale from a masked sum
+// Exact-sum partials of |W| (n4 float4) into `partials` on `grid` CTAs; with
+// mask_gamma, only weights with |w| > fp32(factor x *mask_gamma) count.
+cudaError_t launch_absum(const float4* w4, uint64_t n4, uint32_t* partials, const float* mask_gamma, float factor,
+                         unsigned grid, cudaStream_t s);
+int absum_ctas_per_sm(bool masked);   // 0: the shared memory cannot be reserved
 cudaError_t take_pack_wait_error(int* flag);
 __global__ void bl_gamma_finalize(const uint32_t* __restrict__ partials, int n_partials, uint64_t count,
                                   float* __restrict__ gamma);
-// Codes and packing of W (n_bytes = N*K/4 output bytes) on a one-wave grid.
-// With partials (the fused form) every CTA combines gamma from the
-// exact-sum partials and CTA 0 writes it to *gamma; otherwise gamma is read.
-cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, float* gamma, const uint32_t* partials,
-                              int n_partials, uint32_t* wp_words, int sms, cudaStream_t s);
+// Codes and packing of W (n_bytes = N*K/4 output bytes) on a one-wave grid,
+// by `rule` (kRule*). With partials (the fused form) every CTA combines gamma
+// from the exact-sum partials; otherwise gamma is read from *gamma_in. If
+// scale_out is not null, CTA 0 writes the forward's scale there (gamma or
+// alpha; never for kRuleThreshold).
+cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, const float* gamma_in, const uint32_t* partials,
+                              int n_partials, float* scale_out, uint32_t* wp_words, int rule, float factor, int sms,
+                              cudaStream_t s);
 
 // ---- activation quantisation (act_quant.cu)
 constexpr int kActThreads = 256;

@@ -97,8 +97,12 @@ BL_DEVICE uint32_t pow2_wrap(uint32_t s) {
   return r;
 }
 
+// MASKED: only weights with |w| > delta = fp32(factor x gamma) are summed
+// (gamma read from *gamma_in), for the threshold quantiser's scale.
+template <bool MASKED>
 __global__ void __launch_bounds__(kAbsumThreads + 32, 2)
-bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials) {
+bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restrict__ partials,
+                  const float* __restrict__ gamma_in, float factor) {
   extern __shared__ __align__(128) float4 s_ring[];        // kRingStages x kRingStageF4
   __shared__ unsigned long long s_bins[kBins];
   __shared__ unsigned long long s_limbs[kSmemLimbs];
@@ -142,11 +146,15 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
   } else {
     // ---- consumers: thread t sums float4 t, t + kAbsumThreads, ... of every stage
     uint32_t bias = 0u;
+    // the mask threshold as bits: for non-negative floats the bit patterns
+    // order like the values
+    const uint32_t dbits = MASKED ? __float_as_uint(__fmul_rn(factor, *launder(gamma_in))) : 0u;
+    auto kept = [&](uint32_t abs_bits) { return !MASKED || abs_bits > dbits; };
     // out-of-window weights of a float4 (rare): exact per-exponent bins
     auto rare = [&](float x) {
       const uint32_t b = __float_as_uint(x) & 0x7fffffffu;
       const uint32_t e = b >> 23;
-      if ((e - bias) >= 32u && b != 0u) {
+      if ((e - bias) >= 32u && b != 0u && kept(b)) {
         const uint32_t m = e ? ((b & 0x7fffffu) | 0x800000u) : b;
         atomicAdd(&s_bins[e ? e - 1u : 0u], static_cast<unsigned long long>(m));
       }
@@ -160,18 +168,22 @@ bl_absum_partials(const float4* __restrict__ w4, uint64_t n4, uint32_t* __restri
       const uint32_t b0 = __float_as_uint(v.x), b1 = __float_as_uint(v.y);
       const uint32_t b2 = __float_as_uint(v.z), b3 = __float_as_uint(v.w);
       const uint32_t d0 = (b0 >> 23) - bias, d1 = (b1 >> 23) - bias, d2 = (b2 >> 23) - bias, d3 = (b3 >> 23) - bias;
-      acc = mad_wide_u32((b0 & 0x7fffffu) | 0x800000u, pow2_wrap(d0), acc);
-      acc = mad_wide_u32((b1 & 0x7fffffu) | 0x800000u, pow2_wrap(d1), acc);
-      acc = mad_wide_u32((b2 & 0x7fffffu) | 0x800000u, pow2_wrap(d2), acc);
-      acc = mad_wide_u32((b3 & 0x7fffffu) | 0x800000u, pow2_wrap(d3), acc);
+      const uint32_t m0 = kept(b0 & 0x7fffffffu) ? (b0 & 0x7fffffu) | 0x800000u : 0u;
+      const uint32_t m1 = kept(b1 & 0x7fffffffu) ? (b1 & 0x7fffffu) | 0x800000u : 0u;
+      const uint32_t m2 = kept(b2 & 0x7fffffffu) ? (b2 & 0x7fffffu) | 0x800000u : 0u;
+      const uint32_t m3 = kept(b3 & 0x7fffffffu) ? (b3 & 0x7fffffu) | 0x800000u : 0u;
+      acc = mad_wide_u32(m0, pow2_wrap(d0), acc);
+      acc = mad_wide_u32(m1, pow2_wrap(d1), acc);
+      acc = mad_wide_u32(m2, pow2_wrap(d2), acc);
+      acc = mad_wide_u32(m3, pow2_wrap(d3), acc);
       if ((d0 | d1 | d2 | d3) & 0xe0u) {
         // the four window terms above are exact only for in-window weights:
         // take back those of the others and bin them instead
         const uint32_t dd[4] = {d0, d1, d2, d3};
-        const uint32_t bb[4] = {b0, b1, b2, b3};
+        const uint32_t mm[4] = {m0, m1, m2, m3};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (dd[q] & 0xe0u) acc -= static_cast<unsigned long long>((bb[q] & 0x7fffffu) | 0x800000u) << (dd[q] & 31u);
+          if (dd[q] & 0xe0u) acc -= static_cast<unsigned long long>(mm[q]) << (dd[q] & 31u);
         rare(v.x); rare(v.y); rare(v.z); rare(v.w);
       }
     };
@@ -390,11 +402,23 @@ BL_DEVICE uint32_t pack4(const float4& v, float h) {
          (ternary_field(v.w, h) << 6);
 }
 
+// Code of one weight by the exact quotient: clip(rint(fp32(w / a)), -1, 1)
+// as a packed field (code + 1), for a subnormal divisor a > 0.
+BL_DEVICE uint32_t field_by_division(float w, float a) {
+  const float q = rintf(__fdiv_rn(w, a));
+  return q > 0.f ? 2u : (q < 0.f ? 0u : 1u);
+}
+
+BL_DEVICE uint32_t pack4_division(const float4& v, float a) {
+  return field_by_division(v.x, a) | (field_by_division(v.y, a) << 2) | (field_by_division(v.z, a) << 4) |
+         (field_by_division(v.w, a) << 6);
+}
+
 template <bool FUSED>
 __global__ void __launch_bounds__(kPackThreads + 32, 2)
 bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __restrict__ gamma_in,
               const uint32_t* __restrict__ partials, int n_partials, float* __restrict__ gamma_out,
-              uint32_t* __restrict__ wp_words) {
+              uint32_t* __restrict__ wp_words, int rule, float factor) {
   extern __shared__ __align__(128) float4 s_ring[];        // kRingStages x kRingStageF4
   __shared__ __align__(8) uint64_t s_full[kRingStages], s_empty[kRingStages];
   __shared__ FinalSmem s_fin;
@@ -436,15 +460,34 @@ bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __re
     float g;
     if (FUSED) {
       // every CTA combines the partials itself (while its first stages are in
-      // flight); CTA 0 publishes gamma
+      // flight)
       g = gamma_from_partials(launder(partials), n_partials, n_bytes * 4, s_fin,
                               [] { asm volatile("bar.sync 1, %0;" ::"n"(kPackThreads) : "memory"); });
-      if (blockIdx.x == 0 && tid == 0) *gamma_out = g;
     } else {
       g = *launder(gamma_in);
     }
-    const float d = __fadd_rn(g, kEpsGamma);
-    const float h = 0.5f * d;                 // exact: d is a normal fp32
+    // code = 0 iff |w| <= h, else the sign of w (see ternary_field):
+    //   absmean      h = fp32(gamma + 1e-5) / 2   (exact: a normal fp32 halved)
+    //   alpha-round  h = alpha / 2, alpha = fp32(factor x gamma); below 2^-125
+    //                alpha / 2 may not be exact, so the codes are taken from
+    //                the exact quotient instead; alpha = 0 (an all-zero W)
+    //                gives h = infinity, all codes 0
+    //   threshold    h = delta = fp32(factor x gamma)  (strict |w| > delta)
+    // CTA 0 writes the forward's scale: gamma or alpha (the threshold rule's
+    // scale comes from the masked exact sum).
+    float h, alpha = 0.f;
+    bool divide = false;
+    if (rule == kRuleAlphaRound) {
+      alpha = __fmul_rn(factor, g);
+      divide = alpha > 0.f && alpha < 0x1p-125f;
+      h = alpha > 0.f ? 0.5f * alpha : __int_as_float(0x7f800000);
+    } else if (rule == kRuleThreshold) {
+      h = __fmul_rn(factor, g);
+    } else {
+      h = 0.5f * __fadd_rn(g, kEpsGamma);
+    }
+    if (gamma_out && blockIdx.x == 0 && tid == 0 && rule != kRuleThreshold)
+      *gamma_out = rule == kRuleAlphaRound ? alpha : g;
     // Thread t packs word t of each stage from float4 4t .. 4t + 3, taking
     // them in the rotated order (k + t/2) mod 4, so that the eight threads of
     // each quarter-warp read eight different 16-byte bank groups.
@@ -460,10 +503,14 @@ bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __re
       const float4* st = s_ring + s * kRingStageF4 + 4 * tid;
       uint32_t r = 0u;
       if (mine) {
+        if (!divide) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int q = (k + rot) & 3;
-          r |= pack4(st[q], h) << (8 * q);
+          for (int k = 0; k < 4; ++k) {
+            const int q = (k + rot) & 3;
+            r |= pack4(st[q], h) << (8 * q);
+          }
+        } else {
+          for (int q = 0; q < 4; ++q) r |= pack4_division(st[q], alpha) << (8 * q);
         }
       }
       __syncwarp();
@@ -472,13 +519,18 @@ bl_quant_pack(const float4* __restrict__ w4, uint64_t n_bytes, const float* __re
     }
     // tail: up to three bytes when N*K/4 is not a multiple of 4
     const uint64_t tb = n_words * 4 + static_cast<uint64_t>(blockIdx.x) * kPackThreads + tid;
-    if (tb < n_bytes) reinterpret_cast<uint8_t*>(wp_words)[tb] = static_cast<uint8_t>(pack4(launder(w4)[tb], h));
+    if (tb < n_bytes) {
+      const float4 v = launder(w4)[tb];
+      reinterpret_cast<uint8_t*>(wp_words)[tb] =
+          static_cast<uint8_t>(divide ? pack4_division(v, alpha) : pack4(v, h));
+    }
   }
   if (!ok) atomicExch(&g_pack_wait_error, 1);
 }
 
-cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, float* gamma, const uint32_t* partials,
-                              int n_partials, uint32_t* wp_words, int sms, cudaStream_t s) {
+cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, const float* gamma_in, const uint32_t* partials,
+                              int n_partials, float* scale_out, uint32_t* wp_words, int rule, float factor, int sms,
+                              cudaStream_t s) {
   const bool fused = partials != nullptr;
   auto kern = fused ? bl_quant_pack<true> : bl_quant_pack<false>;
   // resident CTAs per SM of each form (0: the shared memory cannot be reserved)
@@ -500,7 +552,30 @@ cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, float* gamma, 
   uint64_t grid = stages < wave ? stages : wave;
   if (grid < 1) grid = 1;
   return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kPackThreads + 32), kRingSmem, s, w4, n_bytes,
-                    static_cast<const float*>(gamma), partials, n_partials, gamma, wp_words);
+                    gamma_in, partials, n_partials, scale_out, wp_words, rule, factor);
+}
+
+int absum_ctas_per_sm(bool masked) {
+  auto per_sm_of = [](const void* k) {
+    int n = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRingSmem)) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kAbsumThreads + 32, kRingSmem) != cudaSuccess)
+      n = 0;
+    return n;
+  };
+  static const int plain = per_sm_of(reinterpret_cast<const void*>(bl_absum_partials<false>));
+  static const int masked_n = per_sm_of(reinterpret_cast<const void*>(bl_absum_partials<true>));
+  return masked ? masked_n : plain;
+}
+
+cudaError_t launch_absum(const float4* w4, uint64_t n4, uint32_t* partials, const float* mask_gamma, float factor,
+                         unsigned grid, cudaStream_t s) {
+  if (mask_gamma)
+    return launch_pdl(bl_absum_partials<true>, dim3(grid), dim3(kAbsumThreads + 32), kRingSmem, s, w4, n4, partials,
+                      mask_gamma, factor);
+  return launch_pdl(bl_absum_partials<false>, dim3(grid), dim3(kAbsumThreads + 32), kRingSmem, s, w4, n4, partials,
+                    static_cast<const float*>(nullptr), 0.f);
 }
 
 }  // namespace bl

@@ -118,6 +118,45 @@ BL_API bl_status bitlinear_absmean(const float* W, int64_t N, int64_t K, float* 
 BL_API bl_status bitlinear_quantize_pack(const float* W, int64_t N, int64_t K, const float* gamma,
                                          uint8_t* Wp, bl_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Weight packing by one of the quantisers the pages describe. The packed
+ * layout and the forward are unchanged: pass `scale` to bitlinear_forward in
+ * place of gamma (y = acc * scale / s).
+ *
+ *   BL_QUANT_ABSMEAN      the default rule, exactly bitlinear_pack_weights
+ *                         (factor is ignored; scale = gamma).
+ *   BL_QUANT_ALPHA_ROUND  alpha = fp32(factor x mean|W|);
+ *                         code = clip(rint(fp32(W / alpha)), -1, 1); scale = alpha.
+ *                         "BitNet 中使用直通估计器工程化三元权重训练", sections
+ *                         "STE 机制在三元训练中的作用" and "工程化训练流程与参数配置"
+ *                         (factor 0.7; its zero threshold tau = 0.1 alpha changes
+ *                         no code, since |W| < tau already rounds to 0). An
+ *                         all-zero W gives alpha = 0 and all codes 0.
+ *   BL_QUANT_THRESHOLD    delta = fp32(factor x mean|W|); code = sign(W) where
+ *                         |W| > delta, else 0; scale = exact sum of |W| over the
+ *                         kept weights / (N*K), rounded once to fp32.
+ *                         "BitNet 三元权重阈值优化工程实践", section
+ *                         "三元权重阈值优化的核心原理" and its threshold module
+ *                         (factor 0.7; 0.75 for attention, 0.6 for FFN layers).
+ *
+ * mean|W| is gamma of the default rule (the exact mean rounded once to fp32).
+ * factor: positive and finite (the pages use 0.6, 0.7 and 0.75).
+ * Wp, scale, workspace: as Wp, gamma and workspace of bitlinear_pack_weights.
+ * The threshold rule reads W three times and uses *scale for gamma until its
+ * last kernel writes the scale.
+ * ------------------------------------------------------------------------- */
+typedef enum {
+    BL_QUANT_ABSMEAN = 0,
+    BL_QUANT_ALPHA_ROUND = 1,
+    BL_QUANT_THRESHOLD = 2
+} bl_quantizer;
+
+BL_API bl_status bitlinear_pack_weights_quantizer(const float* W, int64_t N, int64_t K,
+                                                  bl_quantizer quantizer, float factor,
+                                                  uint8_t* Wp, float* scale,
+                                                  void* workspace, size_t ws_bytes,
+                                                  bl_stream_t stream);
+
 /* bitlinear_pack_weights_noalloc: the same packing as bitlinear_pack_weights,
  * for callers that cannot allocate device memory and so cannot pass a
  * workspace: a plugin running inside another framework whose caching

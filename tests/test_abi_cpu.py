@@ -79,6 +79,22 @@ def test_pack_rejects_null_misaligned_and_workspace(blt):
     assert lib.bitlinear_pack_weights(16, 64, 64, 16, 16, 256, ws - 1, None) == blt.BL_ERR_WORKSPACE
 
 
+def test_pack_quantizer_rejects_bad_args_on_host(blt):
+    lib = blt.lib
+    ws = lib.bitlinear_pack_workspace_bytes(64, 64)
+    f = lib.bitlinear_pack_weights_quantizer
+    assert f(16, 64, 64, 3, 0.7, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG        # unknown quantizer
+    assert f(16, 64, 64, -1, 0.7, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    for bad in (0.0, -0.7, float("inf"), float("nan")):
+        assert f(16, 64, 64, 1, bad, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG     # factor
+        assert f(16, 64, 64, 2, bad, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG
+    assert f(16, 64, 64, 2, 0.7, None, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG       # Wp
+    assert f(16, 64, 64, 2, 0.7, 16, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG       # scale
+    assert f(16, 64, 62, 2, 0.7, 16, 16, 256, ws, None) == blt.BL_ERR_INVALID_ARG         # K % 4
+    assert f(16, 64, 64, 2, 0.7, 16, 16, 256, ws - 1, None) == blt.BL_ERR_WORKSPACE
+    assert blt.QUANTIZERS == {"absmean": 0, "alpha_round": 1, "threshold": 2}
+
+
 def test_forward_and_quant_reject_bad_args_on_host(blt):
     lib = blt.lib
     ws = lib.bitlinear_forward_workspace_bytes(4, 64, 64)

@@ -159,6 +159,54 @@ def test_absmean_then_quantize_pack_match_pack_weights(n, k):
     np.testing.assert_array_equal(packed.wp.cpu().numpy(), wp_ref)
 
 
+# ------------------------------------------------------------------ the pages' variant quantisers
+_VARIANT = {"alpha_round": oracle.alpha_round_quantize, "threshold": oracle.threshold_quantize}
+
+
+def _check_variant(w, quantizer, factor, x=None):
+    """Codes (packed bytes) and scale bit-exact; with x, the forward with that scale too."""
+    codes, scale = _VARIANT[quantizer](w.numpy(), np.float32(factor))
+    packed = blt.pack_weights(w.cuda(), quantizer=quantizer, factor=factor)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(packed.wp.cpu().numpy(), oracle.pack_codes(codes))
+    assert bits(packed.gamma.cpu().numpy()[0]) == bits(scale), (quantizer, factor)
+    if x is not None:
+        y, xq, s = blt.forward(x.cuda(), packed, return_quant=True)
+        torch.cuda.synchronize()
+        xq_ref, s_ref = oracle.quant_act(x_to_oracle(x))
+        y_ref = oracle.rescale(oracle.ternary_int8_matmul(xq_ref, codes), scale, s_ref)
+        np.testing.assert_array_equal(xq.cpu().numpy(), xq_ref)
+        np.testing.assert_array_equal(bits(y.cpu().numpy()), bits(y_ref))
+
+
+@pytest.mark.parametrize("quantizer", ["alpha_round", "threshold"])
+@pytest.mark.parametrize("factor", [0.7, 0.6, 0.75])
+@pytest.mark.parametrize("n,k", [(3, 12), (257, 1028), (2048, 2560)])
+def test_variant_quantizers_match_oracle(quantizer, factor, n, k):
+    w = gaussian_weights(n, k, seed=n * 7 + k)
+    x = gaussian_activations(3, k, seed=k) if n * k <= 300_000 else None
+    _check_variant(w, quantizer, factor, x)
+
+
+@pytest.mark.parametrize("quantizer", ["alpha_round", "threshold"])
+def test_variant_quantizers_special_weights(quantizer):
+    # Student-t weights and an outlier token through the tensor-core forward
+    _check_variant(student_t_weights(96, 1024, seed=21), quantizer, 0.7,
+                   gaussian_activations(80, 1024, seed=22).to(torch.bfloat16))
+    # tiny weights: alpha below 2^-125, where the codes come from the exact quotient
+    _check_variant((gaussian_weights(16, 256, seed=23) * 1e-36).to(torch.float32), quantizer, 0.7)
+    # an all-zero tensor: scale 0, all codes 0
+    _check_variant(torch.zeros(8, 64), quantizer, 0.7)
+    # elements exactly at the thresholds (alpha / 2 and delta), found on the host
+    w = gaussian_weights(64, 256, seed=24).numpy()
+    for _ in range(4):
+        t = oracle.scaled_mean(w)
+        w[0, 0] = np.float32(t * np.float32(0.5)) if quantizer == "alpha_round" else t
+        w[0, 1] = -w[0, 0]
+    assert oracle.scaled_mean(w) == t
+    _check_variant(torch.from_numpy(w.copy()), quantizer, 0.7)
+
+
 # ------------------------------------------------------------------ invariants of the device path
 def test_pack_is_deterministic_and_order_free():
     w = gaussian_weights(512, 1024, seed=15)
