@@ -495,14 +495,17 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // int8 codes, the token sum of the codes, and the fp16 operand (transposed
 // 16-code blocks, slot 16q + 4i + j = x_q[16q + 4j + i] * 4^-i).
 //
-// One warp per token, eight tokens per CTA. Lane l takes 16-code blocks l,
-// l + 32, ...; the first kCache of them stay in registers between the absmax
-// reduction (warp shuffles only) and the quantisation. Codes are rounded
-// with the 1.5 * 2^23 addition (exact round-to-nearest-even for |v| <= 2^22
-// after the clamp), which also leaves the code in the low mantissa byte.
+// One CTA of kPermThreads per token. Thread t takes 16-code blocks t,
+// t + kPermThreads, ...; the first kPermCache of them (every block up to
+// K = 16384) stay in registers between the absmax reduction (warp shuffles,
+// then one CTA barrier) and the quantisation, so x is read from memory once.
+// Codes are rounded with the 1.5 * 2^23 addition (exact round-to-nearest-even
+// for |v| <= 2^22 after the clamp), which also leaves the code in the low
+// mantissa byte.
 namespace {
 
-constexpr int kPermCache = 4;                // 16-code blocks per lane kept in registers
+constexpr int kPermThreads = 256;            // threads per token
+constexpr int kPermCache = 4;                // 16-code blocks per thread kept in registers
 
 // Raw 16-activation block: 2 (bf16) or 4 (fp32) 16-byte vectors.
 template <int XIN> struct Raw16 {
@@ -572,10 +575,12 @@ BL_DEVICE float code_f(float x, float s) {
 }  // namespace
 
 template <int XIN>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kPermThreads)
 bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int M, int K,
             int8_t* __restrict__ xq_out, float* __restrict__ scale_out, __half* __restrict__ xperm,
             int* __restrict__ rowsum, uint4* __restrict__ zero, size_t zero_n16) {
+  __shared__ float s_max[kPermThreads / 32];
+  __shared__ int s_sum[kPermThreads / 32];
   pdl_wait();
   pdl_launch_dependents();
   x = launder(x);
@@ -585,16 +590,16 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
   for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_n16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x)
     zero[i] = make_uint4(0u, 0u, 0u, 0u);
-  const int lane = threadIdx.x & 31;
-  const int m = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (m >= M) return;
+  const int m = blockIdx.x;                      // one CTA per token
+  if (m >= M) return;                            // uniform over the CTA
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nblk = K >> 4;
   const size_t row = static_cast<size_t>(m) * K;
   __half* xp_row = xperm + row;
   int sum = 0;
   if constexpr (XIN == kXinI8) {
     const int8_t* xr = static_cast<const int8_t*>(x) + row;
-    for (int b = lane; b < nblk; b += 32) {
+    for (int b = tid; b < nblk; b += kPermThreads) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr) + b);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
       float q[16];
@@ -608,7 +613,7 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
     float amax = 0.f;
 #pragma unroll
     for (int c = 0; c < kPermCache; ++c) {
-      const int b = lane + 32 * c;
+      const int b = tid + kPermThreads * c;
       if (b < nblk) {
         cache[c].load(x, row + 16 * b);
         float f[16];
@@ -617,7 +622,7 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
         for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
       }
     }
-    for (int b = lane + 32 * kPermCache; b < nblk; b += 32) {
+    for (int b = tid + kPermThreads * kPermCache; b < nblk; b += kPermThreads) {
       Raw16<XIN> r;
       r.load(x, row + 16 * b);
       float f[16];
@@ -626,12 +631,17 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
       for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
     }
     amax = warp_max(amax);
-    const float s = token_scale(amax);
-    if (lane == 0 && scale_out) scale_out[m] = s;
+    if (lane == 0) s_max[warp] = amax;
+    __syncthreads();
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPermThreads / 32; ++w) a = fmaxf(a, s_max[w]);
+    const float s = token_scale(a);
+    if (tid == 0 && scale_out) scale_out[m] = s;
     int8_t* xq_row = xq_out ? xq_out + row : nullptr;
 #pragma unroll
     for (int c = 0; c < kPermCache; ++c) {
-      const int b = lane + 32 * c;
+      const int b = tid + kPermThreads * c;
       if (b < nblk) {
         float f[16], q[16];
         cache[c].widen(f);
@@ -640,7 +650,7 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
         emit_block(q, xq_row, xp_row, b, xq_out != nullptr, sum);
       }
     }
-    for (int b = lane + 32 * kPermCache; b < nblk; b += 32) {
+    for (int b = tid + kPermThreads * kPermCache; b < nblk; b += kPermThreads) {
       Raw16<XIN> r;
       r.load(x, row + 16 * b);
       float f[16], q[16];
@@ -651,7 +661,14 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
     }
   }
   sum = warp_sum(sum);
-  if (lane == 0) rowsum[m] = sum;
+  if (lane == 0) s_sum[warp] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kPermThreads / 32; ++w) t += s_sum[w];
+    rowsum[m] = t;
+  }
 }
 
 namespace {
@@ -777,14 +794,14 @@ cudaError_t launch_act_perm(const void* x, int xin, const float* scale_in, int M
   __half* xp = static_cast<__half*>(xperm);
   uint4* z = static_cast<uint4*>(zero);
   const size_t n16 = zero_bytes / 16;
-  const int grid = (M + 7) / 8;
+  const int grid = M;
   if (xin == kXinF32)
-    return launch_pdl(bl_act_perm<kXinF32>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
+    return launch_pdl(bl_act_perm<kXinF32>, dim3(grid), dim3(kPermThreads), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
                       rowsum, z, n16);
   if (xin == kXinBF16)
-    return launch_pdl(bl_act_perm<kXinBF16>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
+    return launch_pdl(bl_act_perm<kXinBF16>, dim3(grid), dim3(kPermThreads), 0, s, x, scale_in, M, K, xq_out, scale_out, xp,
                       rowsum, z, n16);
-  return launch_pdl(bl_act_perm<kXinI8>, dim3(grid), dim3(256), 0, s, x, scale_in, M, K, xq_out, scale_out, xp, rowsum,
+  return launch_pdl(bl_act_perm<kXinI8>, dim3(grid), dim3(kPermThreads), 0, s, x, scale_in, M, K, xq_out, scale_out, xp, rowsum,
                     z, n16);
 }
 
