@@ -71,7 +71,7 @@ def test_stack_7b_last_layer_prefill_sampled(proj):
 @pytest.mark.parametrize("m,n,k", [
     (1, 1, 4), (1, 3, 8), (2, 5, 12), (3, 7, 100), (5, 9, 64), (4, 33, 192), (2, 17, 1028),
     (7, 65, 320), (9, 31, 4096), (1, 130, 65536), (4, 64, 65536), (17, 129, 960), (64, 300, 2560),
-    (65, 257, 128), (129, 96, 1088),
+    (65, 257, 128), (129, 96, 1088), (33, 70, 100), (17, 9, 1028),
 ])
 @pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float32])
 def test_shapes(m, n, k, xdt):
