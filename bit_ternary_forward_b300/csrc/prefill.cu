@@ -497,14 +497,14 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 //
 // One CTA of kPermThreads per token. Thread t takes 16-code blocks t,
 // t + kPermThreads, ...; the first kPermCache of them (every block up to
-// K = 16384) stay in registers between the absmax reduction (warp shuffles,
+// K = 8192) stay in registers between the absmax reduction (warp shuffles,
 // then one CTA barrier) and the quantisation, so x is read from memory once.
 // Codes are rounded with the 1.5 * 2^23 addition (exact round-to-nearest-even
 // for |v| <= 2^22 after the clamp), which also leaves the code in the low
 // mantissa byte.
 namespace {
 
-constexpr int kPermThreads = 256;            // threads per token
+constexpr int kPermThreads = 128;            // threads per token
 constexpr int kPermCache = 4;                // 16-code blocks per thread kept in registers
 
 // Raw 16-activation block: 2 (bf16) or 4 (fp32) 16-byte vectors.
