@@ -1,5 +1,6 @@
 // Decode and skinny contraction: packed ternary weights x int8 activations on
-// the warp-level integer tensor-core MMA, for a few tokens (M <= 64).
+// the warp-level integer tensor-core MMA, for a few tokens (5 <= M <= 16 with
+// K % 64 == 0; from M = 17 the tcgen05 path of prefill.cu is faster).
 //
 // Passages: "穿越1比特的奇幻旅程" (2B4T summary), section "GPU端：CUDA内核的定制
 // 魔法" (W1.58A8 matmul over four-per-byte packed weights: pack, store, load,

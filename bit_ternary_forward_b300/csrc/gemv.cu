@@ -1,4 +1,5 @@
-// Decode GEMV: packed-ternary weights x int8 activations for a few tokens.
+// GEMV for any K % 4 == 0: packed-ternary weights x int8 activations, the
+// path for shapes the other contraction kernels do not take (K % 64 != 0).
 //
 // Passages: "穿越1比特的奇幻旅程" (2B4T summary), section "GPU端：CUDA内核的定制
 // 魔法" (W1.58A8 matmul over four-per-byte packed weights: pack, store, load,

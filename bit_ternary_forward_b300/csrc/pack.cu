@@ -13,25 +13,35 @@
 // units (below 2^309 for N*K < 2^32); the kernels below compute it without any
 // rounding, in an order-independent way, then divide by N*K and round once.
 //
+// Both weight passes stream W through four 16 KB shared-memory stages that
+// one producer thread fills with bulk asynchronous copies (ring_produce in
+// async.cuh); the consumer warps sleep on the stage barriers.
+//
 //   1. bl_absum_partials: each CTA sums its share of |W| exactly. Each warp
 //      picks a window of 32 binades from the largest exponent among its first
 //      128 weights (4 binades above it, 27 below). For a weight in the window,
 //      at distance d binades above its bottom, |w| = m * 2^d window units (m
 //      the 24-bit significand), which one wide multiply-add (mad.wide.u32)
-//      adds to a 64-bit register accumulator; 2^d comes from a shift that
-//      gives 0 for any d outside 0..31, so out-of-window weights add nothing
-//      there. One OR over the four shift amounts of a float4 finds those
-//      weights (zeros, subnormals, stragglers far from the warp's scale);
-//      they go to 254 per-exponent 64-bit bins in shared memory. The 64-bit
-//      accumulator is folded into 96 bits after every 16 weights, and the CTA
-//      folds everything into a 384-bit fixed-point partial (12 x 32-bit limbs).
-//   2. bl_gamma_finalize: one CTA adds the partials (shuffle reductions), then
-//      one thread divides the top 64 bits of the exact sum by N*K and rounds
-//      the quotient to fp32, ties to even, with the dropped bits and the
-//      remainder as the sticky bit.
-//   3. bl_quant_pack: codes and packing. code = 0 iff |w| <= d/2 with
-//      d = fp32(gamma + 1e-5), which equals clip(rint(fp32(w/d)), -1, 1) for
-//      every finite w (see ternary_field in common.cuh).
+//      adds to a 64-bit register accumulator; 2^d comes from a wrapping
+//      funnel shift, so the sign bit needs no masking (it adds 256, a
+//      multiple of 32, to the shift amount). One OR over the four shift
+//      amounts of a float4 finds the weights outside the window (zeros,
+//      subnormals, stragglers far from the warp's scale); their terms are
+//      taken back and they go to 254 per-exponent 64-bit bins in shared
+//      memory. The accumulators are folded into 96 bits after every stage,
+//      and the CTA folds everything into a 384-bit fixed-point partial
+//      (12 x 32-bit limbs). The masked form sums only |w| > delta (the
+//      threshold quantiser's scale).
+//   2. The combine adds the partials (shuffle reductions), then one thread
+//      divides the top 64 bits of the exact sum by N*K and rounds the quotient
+//      to fp32, ties to even, with the dropped bits and the remainder as the
+//      sticky bit: inside every CTA of the fused packing pass, or in the
+//      one-CTA bl_gamma_finalize.
+//   3. bl_quant_pack: codes and packing. code = 0 iff |w| <= h, else the sign
+//      of w, with h = fp32(gamma + 1e-5) / 2 for the absmean rule, which equals
+//      clip(rint(fp32(w/d)), -1, 1) with d = fp32(gamma + 1e-5) for every
+//      finite w (see ternary_field in common.cuh); the variant rules change h
+//      (see the kernel).
 
 #include "async.cuh"
 #include "common.cuh"
