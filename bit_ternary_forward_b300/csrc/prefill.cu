@@ -171,11 +171,14 @@ BL_DEVICE float div_rn_markstein(float t, float s, float r) {
 
 }  // namespace
 
-// Work of CTA b (of G): whole tiles b, b + G, ... below dp_tiles, then a run
-// of the k-stages of the split tiles [dp_tiles, dp_tiles + sk_tiles): their
-// sk_tiles * k_iters stages are cut into sk_ctas equal runs, run b for CTA
-// b < sk_ctas. A run is shorter than one tile's stages, so it covers at most
-// the end of one tile and the start of the next.
+// Work of CTA b (of G): first a run of the k-stages of the split tiles
+// [dp_tiles, dp_tiles + sk_tiles) (their sk_tiles * k_iters stages are cut
+// into sk_ctas equal runs, run b for CTA b < sk_ctas; a run is shorter than
+// one tile's stages, so it covers at most the end of one tile and the start
+// of the next), then whole tiles b, b + G, ... below dp_tiles. Split work
+// first: its atomic partials and the final epilogue of a completed split
+// tile then overlap the MMA of the next whole tile instead of ending the
+// kernel.
 struct TcSched {
   int n_tiles_n;   // tiles along the weight rows
   int k_iters;     // k-stages per tile
@@ -191,24 +194,27 @@ struct TcSched {
       u1 = U * (b + 1) / sk_ctas;
     }
   }
-  BL_DEVICE int items(int b, int G) const {
-    const int dp = b < dp_tiles ? (dp_tiles - b + G - 1) / G : 0;
+  BL_DEVICE int split_items(int b) const {
     long long u0, u1;
     run(b, u0, u1);
-    return dp + (u1 > u0 ? static_cast<int>((u1 - 1) / k_iters - u0 / k_iters) + 1 : 0);
+    return u1 > u0 ? static_cast<int>((u1 - 1) / k_iters - u0 / k_iters) + 1 : 0;
+  }
+  BL_DEVICE int items(int b, int G) const {
+    const int dp = b < dp_tiles ? (dp_tiles - b + G - 1) / G : 0;
+    return split_items(b) + dp;
   }
   // item i of CTA b: tile and k-stage range [k0, k1)
   BL_DEVICE void item(int b, int G, int i, int& tile, int& k0, int& k1) const {
-    const int dp = b < dp_tiles ? (dp_tiles - b + G - 1) / G : 0;
-    if (i < dp) {
-      tile = b + i * G;
+    const int ns = split_items(b);
+    if (i >= ns) {
+      tile = b + (i - ns) * G;
       k0 = 0;
       k1 = k_iters;
       return;
     }
     long long u0, u1;
     run(b, u0, u1);
-    const long long t = u0 / k_iters + (i - dp);
+    const long long t = u0 / k_iters + i;
     const long long lo = t * k_iters;
     k0 = static_cast<int>(u0 > lo ? u0 - lo : 0);
     k1 = static_cast<int>(u1 - lo < k_iters ? u1 - lo : k_iters);
