@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "bitlinear_last_error": (ctypes.c_char_p, []),
         "bitlinear_version": (ctypes.c_int, []),
         "bitlinear_device_error": (st, [ctypes.POINTER(ctypes.c_int)]),
+        "bitlinear_tc_schedule": (st, [i64, i64, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -265,6 +266,36 @@ def device_error() -> int:
     return int(flag.value)
 
 
+class TcPlan(NamedTuple):
+    """Launch plan of the tensor-core contraction (see bitlinear_tc_schedule)."""
+
+    bn: int            # tokens per tile
+    grid: int          # CTAs
+    row_tiles: int     # tiles along the weight rows, ceil(N / 128)
+    k_iters: int       # k-stages of 64 per tile
+    dp_tiles: int      # tiles computed whole
+    sk_tiles: int      # tiles split by k-stages
+    sk_ctas: int       # CTAs that take a run of split stages
+    token_tiles: int   # ceil(M / bn)
+    sk_bytes: int      # split-tile buffer and counters in the workspace
+
+
+def tc_schedule(M: int, N: int, K: int, sms: int):
+    """(plan, items): the tensor-core contraction's plan for M x N x K on `sms`
+    SMs and, per CTA, its work items (tile, k0, k1) in execution order. Host
+    arithmetic in the library; no GPU is needed."""
+    plan = (ctypes.c_int32 * 9)()
+    _check("bitlinear_tc_schedule", lib.bitlinear_tc_schedule(M, N, K, sms, plan, None, None, 0))
+    p = TcPlan(*plan)
+    counts = (ctypes.c_int32 * p.grid)()
+    _check("bitlinear_tc_schedule", lib.bitlinear_tc_schedule(M, N, K, sms, plan, counts, None, 0))
+    most = max(counts) if p.grid else 0
+    buf = (ctypes.c_int32 * (p.grid * most * 3))()
+    _check("bitlinear_tc_schedule", lib.bitlinear_tc_schedule(M, N, K, sms, plan, counts, buf, most))
+    items = [[tuple(buf[(b * most + i) * 3:(b * most + i) * 3 + 3]) for i in range(counts[b])] for b in range(p.grid)]
+    return p, items
+
+
 __all__ = ["device_error", "PackedWeight", "BitLinearError", "pack_weights", "absmean", "quantize_pack", "quant_act", "forward",
            "gemm", "gemm_i32",
-           "pack_workspace_bytes", "forward_workspace_bytes", "lib", "LIB_PATH"]
+           "pack_workspace_bytes", "forward_workspace_bytes", "tc_schedule", "TcPlan", "lib", "LIB_PATH"]

@@ -213,6 +213,32 @@ bl_status bitlinear_device_error(int* flag) {
   return BL_OK;
 }
 
+bl_status bitlinear_tc_schedule(int64_t M, int64_t N, int64_t K, int sms, int32_t* plan, int32_t* n_items,
+                                int32_t* items, int max_items) {
+  g_last_error.clear();
+  if (bl_status st = check_dims(M, N, K, true)) return st;
+  if (K % 64) return fail(BL_ERR_INVALID_ARG, "K=%lld is not a multiple of 64", (long long)K);
+  if (sms < 1 || sms > 4096) return fail(BL_ERR_INVALID_ARG, "sms=%d out of range 1..4096", sms);
+  if (!plan) return fail(BL_ERR_INVALID_ARG, "null pointer (plan)");
+  if (items && max_items < 1) return fail(BL_ERR_INVALID_ARG, "max_items=%d must be positive with items", max_items);
+  const bl::TcPlan p = bl::tc_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sms);
+  const int32_t vals[9] = {p.bn,       p.grid,     p.n_tiles_n,
+                           p.k_iters,  p.dp_tiles, p.sk_tiles,
+                           p.sk_ctas,  static_cast<int32_t>((M + p.bn - 1) / p.bn),
+                           static_cast<int32_t>(p.sk_bytes)};
+  for (int i = 0; i < 9; ++i) plan[i] = vals[i];
+  int most = 0;
+  for (int b = 0; b < p.grid; ++b) {
+    const int n = bl::tc_items(p, b, items ? max_items : 0,
+                               items ? items + static_cast<size_t>(b) * max_items * 3 : nullptr);
+    if (n_items) n_items[b] = n;
+    most = n > most ? n : most;
+  }
+  if (items && most > max_items)
+    return fail(BL_ERR_INVALID_ARG, "a CTA has %d work items, more than max_items=%d", most, max_items);
+  return BL_OK;
+}
+
 size_t bitlinear_pack_workspace_bytes(int64_t N, int64_t K) {
   (void)N;
   (void)K;

@@ -7,6 +7,7 @@
 #include "bitlinear.h"
 
 #define BL_DEVICE __device__ __forceinline__
+#define BL_HOST_DEVICE __host__ __device__ __forceinline__
 
 namespace bl {
 

@@ -129,6 +129,10 @@ struct TcPlan {
   size_t sk_buf_bytes = 0, sk_bytes = 0;
 };
 TcPlan tc_plan(int M, int N, int K, int sms);
+// Work items of CTA b of the plan's grid, in the order the kernel computes
+// them: (tile, k0, k1) triples into out[3 i ..] for i < max_items (host
+// arithmetic only). Returns the number of items.
+int tc_items(const TcPlan& plan, int b, int max_items, int32_t* out);
 // x (fp32 / bf16, or int8 x_q with xin == kXinI8) -> fp16 operand xperm [M][K]
 // (transposed 16-code blocks scaled by 4^-i), token sums rowsum [M], and for
 // float input the scales scale_out [M] and optionally int8 codes xq_out; also

@@ -175,12 +175,13 @@ BL_DEVICE float div_rn_markstein(float t, float s, float r) {
 
 // Work of CTA b (of G): first a run of the k-stages of the split tiles
 // [dp_tiles, dp_tiles + sk_tiles) (their sk_tiles * k_iters stages are cut
-// into sk_ctas equal runs, run b for CTA b < sk_ctas; a run is shorter than
-// one tile's stages, so it covers at most the end of one tile and the start
-// of the next), then whole tiles b, b + G, ... below dp_tiles. Split work
-// first: its atomic partials and the final epilogue of a completed split
-// tile then overlap the MMA of the next whole tile instead of ending the
-// kernel.
+// into sk_ctas runs of equal length to within one stage, run b for CTA
+// b < sk_ctas; the part of a run inside one tile is one item, so a run is
+// the end of one tile, any whole tiles, then the start of another), then
+// whole tiles b, b + G, ... below dp_tiles. Split work first: its atomic
+// partials and the final epilogue of a completed split tile then overlap the
+// MMA of the next whole tile instead of ending the kernel. The same code
+// runs on the host to list the schedule (tc_items).
 struct TcSched {
   int n_tiles_n;   // tiles along the weight rows
   int k_iters;     // k-stages per tile
@@ -188,7 +189,7 @@ struct TcSched {
   int sk_tiles;    // tiles split over the CTAs
   int sk_ctas;     // CTAs that take a run of split-tile stages
 
-  BL_DEVICE void run(int b, long long& u0, long long& u1) const {
+  BL_HOST_DEVICE void run(int b, long long& u0, long long& u1) const {
     u0 = u1 = 0;
     if (b < sk_ctas) {
       const long long U = static_cast<long long>(sk_tiles) * k_iters;
@@ -196,17 +197,17 @@ struct TcSched {
       u1 = U * (b + 1) / sk_ctas;
     }
   }
-  BL_DEVICE int split_items(int b) const {
+  BL_HOST_DEVICE int split_items(int b) const {
     long long u0, u1;
     run(b, u0, u1);
     return u1 > u0 ? static_cast<int>((u1 - 1) / k_iters - u0 / k_iters) + 1 : 0;
   }
-  BL_DEVICE int items(int b, int G) const {
+  BL_HOST_DEVICE int items(int b, int G) const {
     const int dp = b < dp_tiles ? (dp_tiles - b + G - 1) / G : 0;
     return split_items(b) + dp;
   }
   // item i of CTA b: tile and k-stage range [k0, k1)
-  BL_DEVICE void item(int b, int G, int i, int& tile, int& k0, int& k1) const {
+  BL_HOST_DEVICE void item(int b, int G, int i, int& tile, int& k0, int& k1) const {
     const int ns = split_items(b);
     if (i >= ns) {
       tile = b + (i - ns) * G;
@@ -756,6 +757,33 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
 
 namespace {
 
+TcSched sched_of(const TcPlan& p) {
+  TcSched sch;
+  sch.n_tiles_n = p.n_tiles_n;
+  sch.k_iters = p.k_iters;
+  sch.dp_tiles = p.dp_tiles;
+  sch.sk_tiles = p.sk_tiles;
+  sch.sk_ctas = p.sk_ctas;
+  return sch;
+}
+
+}  // namespace
+
+int tc_items(const TcPlan& p, int b, int max_items, int32_t* out) {
+  const TcSched sch = sched_of(p);
+  const int n = sch.items(b, p.grid);
+  for (int i = 0; i < n && i < max_items; ++i) {
+    int tile, k0, k1;
+    sch.item(b, p.grid, i, tile, k0, k1);
+    out[3 * i] = tile;
+    out[3 * i + 1] = k0;
+    out[3 * i + 2] = k1;
+  }
+  return n;
+}
+
+namespace {
+
 template <int BN, bool OUT_ACC>
 cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale, const int* rowsum,
                         const float* gamma, void* out, int M, int N, int K, const TcPlan& p, void* sk_ws,
@@ -770,12 +798,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const 
     if (e != cudaSuccess) return e;
     done = smem;
   }
-  TcSched sch;
-  sch.n_tiles_n = p.n_tiles_n;
-  sch.k_iters = p.k_iters;
-  sch.dp_tiles = p.dp_tiles;
-  sch.sk_tiles = p.sk_tiles;
-  sch.sk_ctas = p.sk_ctas;
+  const TcSched sch = sched_of(p);
   float* sk_buf = static_cast<float*>(sk_ws);
   int* sk_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(sk_ws) + p.sk_buf_bytes);
   return launch_pdl(bl_gemm_tc<BN, OUT_ACC>, dim3(p.grid), dim3(kThreads), smem, s, tm_x, tm_w, scale, rowsum, gamma,

@@ -262,6 +262,35 @@ BL_API bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp,
                              bl_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Schedule of the tensor-core contraction (the path of bitlinear_forward,
+ * bitlinear_gemm and bitlinear_gemm_i32 for M >= 17 and K % 64 == 0), as a
+ * test hook: host arithmetic only, no CUDA call, so it runs on any machine.
+ * It lists the work the persistent kernel's CTAs would do for M tokens, N
+ * weight rows and K inputs on `sms` multiprocessors, so that a test can check
+ * that every output tile's k-stages are covered exactly once.
+ *
+ * Output tiles are 128 weight rows x BN tokens; tile t covers weight rows
+ * from 128 (t % R) and tokens from BN (t / R), R = ceil(N / 128), and has
+ * K / 64 k-stages. Tiles below D are computed whole; tiles D .. D + S - 1 are
+ * split by k-stages over several CTAs whose partial sums are added in an
+ * fp32 buffer.
+ *
+ * plan      int32 [9], written: BN, grid (CTAs), R, k-stages per tile, D, S,
+ *           CTAs that take a run of split stages, token tiles ceil(M / BN),
+ *           bytes of the split-tile buffer and counters in the workspace.
+ * n_items   int32 [grid] or NULL: the number of work items of each CTA.
+ * items     int32 [grid][max_items][3] or NULL: item i of CTA b is
+ *           (tile, k0, k1), the tile and its k-stage range [k0, k1), in the
+ *           order the CTA computes them. Caller-owned host memory.
+ * Errors: BL_ERR_INVALID_ARG for sizes bitlinear_forward rejects, K not a
+ * multiple of 64, sms outside 1..4096, a NULL plan, or (with items) a CTA
+ * with more than max_items items; n_items is complete in that last case.
+ * ------------------------------------------------------------------------- */
+BL_API bl_status bitlinear_tc_schedule(int64_t M, int64_t N, int64_t K, int sms,
+                                       int32_t* plan, int32_t* n_items, int32_t* items,
+                                       int max_items);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------- */
 BL_API const char* bitlinear_strerror(bl_status status);   /* static string */
