@@ -172,7 +172,7 @@ bl_status launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const flo
   cudaError_t e = bl::launch_gemv_fused(wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out,
                                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.rows, p.parts,
                                         p.smem, workspace, s);
-  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemv_fused: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_act_tq + bl_gemv_w: %s", cudaGetErrorString(e));
   return BL_OK;
 }
 

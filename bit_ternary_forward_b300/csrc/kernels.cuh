@@ -70,7 +70,6 @@ cudaError_t launch_act_quant(const void* x, bool bf16, int M, int K, int8_t* xq,
 
 // ---- decode GEMV (gemv.cu)
 constexpr int kGemvThreads = 512;          // 16 warps, one output row per warp at a time
-constexpr int kGemvMaxTokens = 4;          // tokens per CTA (grid.y covers larger M)
 
 enum class GemvOut { kY = 0, kAcc = 1 };
 
@@ -119,7 +118,6 @@ cudaError_t take_gemv_wait_error(int* flag);
 // ---- prefill contraction on tcgen05 (prefill.cu)
 constexpr int kTcMinM = 17;   // smallest M routed to the tensor-core kernel (below it the
                               // mma.sync decode kernel is faster on B300)
-size_t gemm_tc_smem_bytes();
 // Launch plan of the tensor-core contraction (tc_plan, prefill.cu): token-tile
 // width, grid, whole tiles and split ("stream-K") tiles, and the bytes of its
 // split-tile workspace (an fp32 buffer of sk_buf_bytes, then int counters),

@@ -48,11 +48,12 @@
 //               accumulator: tcgen05.ld 32x32b (TMEM lane = weight row, one
 //               lane quarter per warp), stores coalesced along the rows.
 // Every wait on the full / expanded / empty stage barriers and on the
-// accumulator barriers is bounded. The producer, expansion and epilogue warps
-// sleep until the phase completes instead of polling: polling warps take
-// issue slots from the MMA thread (measured 4-6 % slower). The MMA thread
-// alone polls its expanded-stage barrier, which is 1-3 % faster than sleeping
-// there, because its wake-up latency delays the next MMAs.
+// accumulator barriers is bounded. The expansion and epilogue warps sleep
+// until the phase completes instead of polling: polling warps take issue
+// slots from the MMA thread (measured 4-6 % slower). The two single threads
+// poll: the MMA thread on its expanded-stage barrier (1-3 % faster than
+// sleeping there, because its wake-up latency delays the next MMAs) and the
+// TMA producer on its free-stage barrier (no measurable difference).
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -294,7 +295,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
         for (int it = k0; it < k1; ++it, ++g) {
           const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
-          if (g >= kStages) ok = mbar_wait_sleep(&empty[s], ph ^ 1u) && ok;
+          if (g >= kStages) ok = mbar_wait(&empty[s], ph ^ 1u) && ok;   // polls (one thread)
           uint8_t* st = smem + s * kStageBytes;
           mbar_expect_tx(&full[s], kXBytes + kWpBytes);
           tma_load_2d(st, &tm_x, it * kBK, m0, &full[s]);
@@ -703,8 +704,6 @@ EncodeTiled encode_fn() {
 }
 
 }  // namespace
-
-size_t gemm_tc_smem_bytes() { return smem_for(kMaxBN); }
 
 // Launch plan: token-tile width BN, grid and work split. For each BN the
 // tiles are dealt round-robin to the SMs; a last round that would occupy at
