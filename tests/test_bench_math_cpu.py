@@ -1,0 +1,125 @@
+"""The bench's measurement arithmetic on the host: algorithmic bytes and
+operations per call, the clock-sample summary that decides whether a run is
+kept, the lookup of the committed DRAM traffic record, and the roofline
+denominators."""
+
+from __future__ import annotations
+
+import json
+import os
+import sys
+from types import SimpleNamespace
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def proj(m, k, n, x_dtype="bf16"):
+    return SimpleNamespace(m=m, k=k, n=n, x_dtype=x_dtype)
+
+
+def test_decode_bytes_of_the_2b_projection():
+    """M=1, K=2560 -> N=6912, bf16 x: packed W 4,423,680 B, x 5,120 B, y
+    27,648 B, gamma 4 B, scale 4 B (4,456,456 B), plus the x_q codes (2,560 B)
+    the forward also writes out."""
+    b = bench.row_bytes(proj(1, 2560, 6912))
+    assert b["forward"] == 4_423_680 + 5_120 + 27_648 + 4 + 4 + 2_560
+    # packing reads the fp32 weight twice (gamma must be complete before any
+    # code) and writes the packed bytes and gamma
+    assert b["pack_weights"] == 2 * 4 * 6912 * 2560 + 6912 * 2560 // 4 + 4
+
+
+def test_fp32_activations_count_four_bytes():
+    assert bench.row_bytes(proj(4, 256, 256, "f32"))["forward"] - bench.row_bytes(proj(4, 256, 256))["forward"] \
+        == 2 * 4 * 256
+
+
+def test_prefill_operations():
+    # 72.48 G operations per 2B-class projection at M = 2048
+    assert bench.row_ops(proj(2048, 2560, 6912))["forward"] == 2 * 2048 * 6912 * 2560 == 72_477_573_120
+    projs = [proj(2048, 2560, 6912), proj(2048, 6912, 2560)]
+    assert bench.workload_units(projs, "TOPS") == 2 * 72_477_573_120
+
+
+def test_workload_units_sums_the_rows():
+    projs = [proj(1, 2560, 6912), proj(1, 6912, 2560)]
+    total = bench.workload_units(projs, "GB/s")
+    by_row = sum(sum(bench.row_bytes(p).values()) for p in projs)
+    assert total == by_row
+    assert bench.workload_units(projs, "GB/s", rows=["forward"]) == sum(bench.row_bytes(p)["forward"] for p in projs)
+
+
+@pytest.mark.parametrize("m,k,want", [
+    (1, 2560, ["bl_act_tq", "bl_gemv_w"]), (4, 2560, ["bl_act_tq", "bl_gemv_w"]),
+    (8, 2560, ["bl_decode_mma"]), (16, 2560, ["bl_act_quant", "bl_decode_mma"]),
+    (17, 2560, ["bl_act_perm", "bl_gemm_tc"]), (2048, 6912, ["bl_act_perm", "bl_gemm_tc"]),
+])
+def test_row_kernels_follow_the_library_dispatch(m, k, want):
+    assert bench.row_kernels(proj(m, k, 6912))["forward"] == want
+
+
+class _Done:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _sampler(rows, t0=10.0, t1=20.0):
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc, s.thread, s.t0, s.t1 = _Done(), None, t0, t1
+    s.samples = [(t, [c.strip() for c in r.split(",")]) for t, r in rows]
+    return s
+
+
+def test_clock_summary_uses_samples_inside_the_timed_region(monkeypatch):
+    monkeypatch.setattr(bench.time, "sleep", lambda _s: None)
+    rows = [
+        (9.0, "1200, 2032, 200.0, 0x0, Not Active, Not Active, Not Active, Not Active"),      # before
+        (11.0, "2032, 2032, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active"),
+        (12.0, "1965, 2032, 1090.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (13.0, "1957, 2032, 1088.0, 0x4, Not Active, Not Active, Not Active, Active"),
+        (25.0, "2032, 2032, 150.0, 0x0, Active, Not Active, Not Active, Not Active"),          # after
+    ]
+    c = _sampler(rows).stop()
+    assert c["samples"] == 3 and c["sm_mhz"] == 1965.0 and c["sm_max_mhz"] == 2032.0
+    assert c["power_w_max"] == 1090.0
+    assert c["reasons"] == ["sw_power_cap"]          # the hw_slowdown sample lies outside
+
+
+def test_clock_summary_reports_every_throttle_reason(monkeypatch):
+    monkeypatch.setattr(bench.time, "sleep", lambda _s: None)
+    rows = [(15.0, "1500, 2032, 700.0, 0x68, Active, Active, Active, Not Active")]
+    c = _sampler(rows).stop()
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_summary_without_nvidia_smi():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc = None
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_traffic_record_is_keyed_to_the_kernel_source(monkeypatch):
+    got = bench.traffic_record("pack_weights", "decode_2b")
+    assert got is not None and got > 8 * 6912 * 2560 * 0.99      # W read twice, per launch
+    assert bench.traffic_record("forward", "prefill_2b", True) is not None
+    assert bench.traffic_record("pack_weights", "no_such_workload") is None
+    monkeypatch.setattr(bench, "source_hash", lambda src: "0000000000000000")
+    assert bench.traffic_record("pack_weights", "decode_2b") is None   # a changed kernel has no record
+
+
+def test_peaks_come_from_the_measured_file():
+    hbm, bf16, sustained, source = bench.peaks()
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        assert source == "fallback" and (hbm, bf16) == (bench.FALLBACK_HBM_GBS, bench.FALLBACK_BF16_TFLOPS)
+        return
+    d = json.load(open(path))
+    assert source == "measured" and hbm == float(d["hbm_gbs"]) and bf16 == float(d["bf16_tflops"])
+    assert sustained <= bf16
