@@ -91,6 +91,25 @@ def _cuda(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
     return t
 
 
+def _same_device(t: torch.Tensor, name: str, device: torch.device) -> torch.Tensor:
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _out(t: torch.Tensor, name: str, dtype, shape, device: torch.device) -> torch.Tensor:
+    """A caller-provided output: checked before the library writes shape-many elements into it."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return _same_device(t, name, device)
+
+
 def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
     """(holder, base, nbytes): a 256-byte aligned region; keep `holder` alive across the call."""
     if nbytes == 0:
@@ -98,9 +117,11 @@ def _workspace(nbytes: int, device, ws: Optional[torch.Tensor]):
     if ws is None:
         # 256 extra bytes so the base can be rounded up to a 256-byte boundary
         ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+    elif ws.device != torch.device(device) or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
     p = ws.data_ptr()
     base = (p + 255) // 256 * 256
-    if base + nbytes > p + ws.numel():
+    if base + nbytes > p + ws.numel() * ws.element_size():
         raise ValueError("workspace tensor too small")
     return ws, base, nbytes
 
@@ -140,6 +161,9 @@ def pack_weights(w: torch.Tensor, out: Optional[PackedWeight] = None,
     if out is None:
         out = PackedWeight(torch.empty((n, k // 4), dtype=torch.uint8, device=w.device),
                            torch.empty(1, dtype=torch.float32, device=w.device), n, k)
+    else:
+        _out(out.wp, "out.wp", torch.uint8, (n, k // 4), w.device)
+        _out(out.gamma, "out.gamma", torch.float32, (1,), w.device)
     hold, ws, wsn = _workspace(pack_workspace_bytes(n, k), w.device, workspace)
     if quantizer == "absmean":
         _check("bitlinear_pack_weights",
@@ -160,6 +184,8 @@ def absmean(w: torch.Tensor, gamma: Optional[torch.Tensor] = None,
     n, k = w.shape
     if gamma is None:
         gamma = torch.empty(1, dtype=torch.float32, device=w.device)
+    else:
+        _out(gamma, "gamma", torch.float32, (1,), w.device)
     hold, ws, wsn = _workspace(pack_workspace_bytes(n, k), w.device, workspace)
     _check("bitlinear_absmean", lib.bitlinear_absmean(w.data_ptr(), n, k, gamma.data_ptr(), ws, wsn,
                                                       _stream(w.device)))
@@ -169,10 +195,12 @@ def absmean(w: torch.Tensor, gamma: Optional[torch.Tensor] = None,
 def quantize_pack(w: torch.Tensor, gamma: torch.Tensor, wp: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Ternary codes of W against a given gamma, packed four per byte: uint8 [N][K/4]."""
     _cuda(w, "W", torch.float32)
-    _cuda(gamma, "gamma", torch.float32)
+    _same_device(_cuda(gamma, "gamma", torch.float32), "gamma", w.device)
     n, k = w.shape
     if wp is None:
         wp = torch.empty((n, k // 4), dtype=torch.uint8, device=w.device)
+    else:
+        _out(wp, "wp", torch.uint8, (n, k // 4), w.device)
     _check("bitlinear_quantize_pack", lib.bitlinear_quantize_pack(w.data_ptr(), n, k, gamma.data_ptr(),
                                                                   wp.data_ptr(), _stream(w.device)))
     return wp
@@ -182,13 +210,17 @@ def gemm(xq: torch.Tensor, scale: torch.Tensor, packed: PackedWeight, y: Optiona
          workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """y = (x_q . codes^T) * gamma / s on already-quantised activations."""
     _cuda(xq, "xq", torch.int8)
-    _cuda(scale, "scale", torch.float32)
     m, k = xq.shape
     if k != packed.k:
         raise ValueError(f"xq must be [M][{packed.k}]")
     n = packed.n
+    _out(_cuda(scale, "scale", torch.float32), "scale", torch.float32, (m,), xq.device)
+    _same_device(packed.wp, "packed.wp", xq.device)
+    _same_device(packed.gamma, "packed.gamma", xq.device)
     if y is None:
         y = torch.empty((m, n), dtype=torch.float32, device=xq.device)
+    else:
+        _out(y, "y", torch.float32, (m, n), xq.device)
     hold, ws, wsn = _workspace(int(lib.bitlinear_gemm_workspace_bytes(m, n, k)), xq.device, workspace)
     _check("bitlinear_gemm", lib.bitlinear_gemm(xq.data_ptr(), scale.data_ptr(), m, packed.wp.data_ptr(),
                                                 packed.gamma.data_ptr(), n, k, y.data_ptr(), ws, wsn,
@@ -211,8 +243,12 @@ def quant_act(x: torch.Tensor, xq: Optional[torch.Tensor] = None,
     m, k = x.shape
     if xq is None:
         xq = torch.empty((m, k), dtype=torch.int8, device=x.device)
+    else:
+        _out(xq, "xq", torch.int8, (m, k), x.device)
     if scale is None:
         scale = torch.empty(m, dtype=torch.float32, device=x.device)
+    else:
+        _out(scale, "scale", torch.float32, (m,), x.device)
     _check("bitlinear_quant_act",
            lib.bitlinear_quant_act(x.data_ptr(), _dtype_code(x), m, k, xq.data_ptr(), scale.data_ptr(),
                                    _stream(x.device)))
@@ -227,8 +263,12 @@ def forward(x: torch.Tensor, packed: PackedWeight, y: Optional[torch.Tensor] = N
         raise ValueError(f"x must be [M][{packed.k}]")
     m, k = x.shape
     n = packed.n
+    _same_device(packed.wp, "packed.wp", x.device)
+    _same_device(packed.gamma, "packed.gamma", x.device)
     if y is None:
         y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    else:
+        _out(y, "y", torch.float32, (m, n), x.device)
     xq = scale = None
     if return_quant:
         xq = torch.empty((m, k), dtype=torch.int8, device=x.device)
@@ -247,10 +287,13 @@ def gemm_i32(xq: torch.Tensor, wp: torch.Tensor, acc: Optional[torch.Tensor] = N
     _cuda(wp, "wp", torch.uint8)
     m, k = xq.shape
     n = wp.shape[0]
-    if wp.shape[1] * 4 != k:
+    if wp.dim() != 2 or wp.shape[1] * 4 != k:
         raise ValueError("wp must be [N][K/4]")
+    _same_device(wp, "wp", xq.device)
     if acc is None:
         acc = torch.empty((m, n), dtype=torch.int32, device=xq.device)
+    else:
+        _out(acc, "acc", torch.int32, (m, n), xq.device)
     wsn_req = int(lib.bitlinear_gemm_i32_workspace_bytes(m, n, k))
     hold, ws, wsn = _workspace(wsn_req, xq.device, None)
     _check("bitlinear_gemm_i32",

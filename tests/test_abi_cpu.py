@@ -116,3 +116,38 @@ def test_python_binding_rejects_cpu_tensors(blt):
         blt.pack_weights(torch.zeros(4, 4))
     with pytest.raises(TypeError):
         blt.quant_act(torch.zeros(4, 4))
+
+
+def test_python_binding_checks_caller_outputs(blt):
+    # the binding checks every caller-provided output before the library
+    # writes into it (the checks use no CUDA call, so CPU tensors show them)
+    import torch
+    cpu = torch.device("cpu")
+    ok = torch.empty((4, 8), dtype=torch.float32)
+    assert blt._out(ok, "y", torch.float32, (4, 8), cpu) is ok
+    with pytest.raises(TypeError):
+        blt._out(ok, "y", torch.int32, (4, 8), cpu)                       # dtype
+    with pytest.raises(ValueError):
+        blt._out(ok, "y", torch.float32, (4, 9), cpu)                     # shape
+    with pytest.raises(ValueError):
+        blt._out(ok.t(), "y", torch.float32, (8, 4), cpu)                 # not contiguous
+    with pytest.raises(ValueError):
+        blt._out(ok, "y", torch.float32, (4, 8), torch.device("cuda", 0))  # another device
+    with pytest.raises(TypeError):
+        blt._out(None, "y", torch.float32, (4, 8), cpu)
+
+
+def test_python_binding_checks_the_workspace(blt):
+    import torch
+    cpu = torch.device("cpu")
+    assert blt._workspace(0, cpu, None) == (None, 0, 0)
+    ws = torch.empty(1024 + 256, dtype=torch.uint8)
+    hold, base, n = blt._workspace(1024, cpu, ws)
+    assert hold is ws and base % 256 == 0 and n == 1024
+    assert base + n <= ws.data_ptr() + ws.numel()
+    wide = torch.empty(320, dtype=torch.float32)                         # 1280 bytes
+    assert blt._workspace(1024, cpu, wide)[2] == 1024
+    with pytest.raises(ValueError):
+        blt._workspace(4096, cpu, ws)                                    # too small
+    with pytest.raises(ValueError):
+        blt._workspace(1024, torch.device("cuda", 0), ws)               # another device
