@@ -218,8 +218,8 @@ BL_API bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int6
  *
  * The kernels are chosen by M and K: with K % 64 == 0, a dp4a GEMV with the
  * activation pass ahead of it for M <= 4, a fused mma.sync kernel for
- * M <= 8, activation quantisation plus mma.sync for M <= 64, and the tcgen05
- * tensor-core path for M >= 65; K % 64 != 0 takes the activation pass plus a
+ * M <= 8, activation quantisation plus mma.sync for M <= 16, and the tcgen05
+ * tensor-core path for M >= 17; K % 64 != 0 takes the activation pass plus a
  * dp4a kernel. Calls that share a workspace must not overlap on the GPU.
  * ------------------------------------------------------------------------- */
 BL_API size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K);
