@@ -135,7 +135,6 @@ def m_rescale_multiply_s(acc, gamma, s):
 
 
 def m_round_ratio_truncate(num, den):
-    import math
     v = ob.round_ratio_to_f32(num, den)
     # truncation toward zero instead of nearest
     from fractions import Fraction
