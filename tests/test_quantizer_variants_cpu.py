@@ -213,3 +213,28 @@ def test_variant_mutant_is_caught(name):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"planted mistake {name} passed every pin"
+
+
+# ---------------------------------------------------------------- generated inputs
+def test_variants_match_rationals_on_generated_tensors():
+    """Both rules against the rational references on generated tiny tensors over
+    every finite fp32 value (subnormals, the largest normals, signed zeros).
+    |w| <= N K mean|W|, so w / alpha stays finite."""
+    from hypothesis import given, settings
+    from hypothesis import strategies as st
+
+    finite32 = st.floats(width=32, allow_nan=False, allow_infinity=False)
+    values = st.one_of(finite32, st.floats(min_value=-1.0, max_value=1.0, width=32))
+
+    @settings(max_examples=300, deadline=None)
+    @given(st.integers(1, 3), st.sampled_from([4, 8]), st.data())
+    def check(n, k, data):
+        w = np.array(data.draw(st.lists(values, min_size=n * k, max_size=n * k)), F32).reshape(n, k)
+        c, a = oracle.alpha_round_quantize(w)
+        rc, ra = _ref_alpha_round(w)
+        assert np.array_equal(c, rc) and F32(a).view(np.uint32) == F32(ra).view(np.uint32)
+        c, a = oracle.threshold_quantize(w)
+        rc, ra = _ref_threshold(w)
+        assert np.array_equal(c, rc) and F32(a).view(np.uint32) == F32(ra).view(np.uint32)
+
+    check()
