@@ -24,7 +24,8 @@ def blt():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"\b(bitlinear_[a-z0-9_]+)\s*\(", text)
     return sorted(set(names))
