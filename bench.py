@@ -1,23 +1,37 @@
 #!/usr/bin/env python
-"""Benchmark of the BitLinear W1.58A8 hot path on one B300 (or N replicas).
+"""Benchmark of the BitLinear W1.58A8 forward on one B300 (or N replicas).
 
-One step runs every step of the path, through the C ABI, on every projection
-of the workload, with inputs resident in HBM:
+The metric has two halves, GB/s for decode and int8-equivalent TOPS for
+prefill, each against its roofline. One default run measures both:
 
-    a1-a3   bitlinear_pack_weights   gamma = mean|W| (exact), ternary codes,
-                                     four per byte (W is read twice: gamma
-                                     must be complete before any code is)
-    a4-a6   bitlinear_forward        per-token absmax int8 activations, ternary x
-                                     int8 contraction, fp32 rescale (x_q and s
-                                     are written out too)
+decode (the line's `value`)
+    One step is bitlinear_forward on every projection of the workload
+    (default decode_2b: M=1, K=2560->N=6912 and K=6912->N=2560, bf16
+    activations) over weights packed once at set-up, as a deployed model's
+    are. Distinct packed-weight buffers totalling at least twice the L2 size
+    are rotated between steps, so every forward streams its packed weights
+    from HBM. Bytes per projection (the algorithmic traffic):
+        N*K/4 (packed W) + xb*M*K (x) + 4*M*N (y) + 4 (gamma) + 4*M (scales).
+prefill (`prefill` object and rows)
+    The same step at M=2048 on the prefill_2b projections; operations
+    2*M*N*K per projection.
+pack_weights (a row)
+    bitlinear_pack_weights (gamma = exact mean|W|, codes, four per byte) is
+    one-time work per layer and sits outside the timed step; its compulsory
+    bytes are 4*N*K + N*K/4 + 4 (W read once), and the measured DRAM traffic
+    (W read twice: gamma must be complete before any code) is reported beside.
 
-The default workload is the 2B-class decode GEMV (M=1, K=2560->N=6912 and
-K=6912->N=2560, fp32 weights packed to 2 bits, bf16 activations). The step
-is captured once in a CUDA graph (external event nodes between the calls give
-each call's device time) and the timed region replays it.
+Each step is captured in a CUDA graph and replayed in the timed region
+(events on the launching stream, barrier and synchronize on both sides). A
+second graph of the same calls with event nodes between them gives each
+call's own device time (the rows). `e2e` repeats the decode step through the
+public Python API with host buffers: every step copies x in from pinned
+memory and y out. `cpu_baseline` times the CPU oracle on a row sample, on one
+core and on every host core.
 
-Prints one JSON line. `--impl reference` times the CPU oracle instead (on the
-host cores, on a bounded sample of the same workload).
+--workload selects another workload (skinny_2b, prefill_2b, stack_7b_decode,
+stack_7b_prefill, cpu_small) as the line's own step; --impl reference times
+the oracle on the host cores instead (the reference arm).
 """
 
 from __future__ import annotations
@@ -25,6 +39,8 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
+import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -43,18 +59,25 @@ from workloads import WORKLOADS, make_projection_inputs  # noqa: E402
 
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
+FALLBACK_L2_BYTES = 126 * 2 ** 20
 METRIC = "BitLinear W1.58A8 GB/s (decode) & int8 TOPS (prefill), % of roofline, 1xB300"
+PREFILL_COMPANION = "prefill_2b"     # the prefill half measured beside the default decode line
 
 
 # --------------------------------------------------------------------------- algorithmic work
+def x_bytes(p):
+    return 2 if p.x_dtype == "bf16" else 4
+
+
 def row_bytes(p):
-    """Compulsory bytes of each call on one projection (inputs read once, outputs written once)."""
+    """Algorithmic bytes of each call on one projection.
+
+    forward: packed W, x and y once, gamma and the per-token scales.
+    pack_weights: the compulsory traffic, W read once, Wp and gamma written."""
     nk, mk, mn = p.n * p.k, p.m * p.k, p.m * p.n
-    xb = 2 if p.x_dtype == "bf16" else 4
     return {
-        "pack_weights": 8 * nk + nk // 4 + 4,                     # read W twice, write Wp and gamma
-        # read x, Wp, gamma; write y and the quantised activations (x_q, s)
-        "forward": xb * mk + nk // 4 + 4 + 4 * mn + mk + 4 * p.m,
+        "forward": nk // 4 + x_bytes(p) * mk + 4 * mn + 4 + 4 * p.m,
+        "pack_weights": 4 * nk + nk // 4 + 4,
     }
 
 
@@ -62,28 +85,29 @@ def row_ops(p):
     return {"forward": 2 * p.m * p.n * p.k}
 
 
-ROWS = ["pack_weights", "forward"]
-FUSED_MAX_M = 8     # the forward quantises activations inside the contraction up to this M
-
-
 def row_kernels(p):
+    """The kernels one call launches, following the library's dispatch."""
     if p.k % 64 == 0 and p.m >= 17:
         fwd = ["bl_act_perm", "bl_gemm_tc"]
     elif p.k % 64 == 0 and p.m <= 4:
         fwd = ["bl_act_tq", "bl_gemv_w"]
-    elif p.k % 64 == 0 and p.m <= FUSED_MAX_M:
+    elif p.k % 64 == 0 and p.m <= 8:
         fwd = ["bl_decode_mma"]
-    else:
+    elif p.k % 64 == 0:
         fwd = ["bl_act_quant", "bl_decode_mma"]
-    return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"],
-            "forward": fwd}
+    else:
+        fwd = ["bl_act_quant", "bl_gemv_w2a8"]
+    return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"], "forward": fwd}
 
 
-def workload_units(projs, unit, rows=None):
-    rows = rows or ROWS
+def workload_units(projs, unit, rows=("forward",)):
     if unit == "GB/s":
-        return sum(sum(v for r, v in row_bytes(p).items() if r in rows) for p in projs)
+        return sum(row_bytes(p)[r] for p in projs for r in rows)
     return sum(row_ops(p)["forward"] for p in projs)
+
+
+def is_decode(wl):
+    return all(p.m <= 64 for p in wl.projections)
 
 
 def peaks():
@@ -94,6 +118,16 @@ def peaks():
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1400.0, "fallback"
+
+
+MAX_ORACLE_PROCESSES = 32   # each process holds its own copy of the sampled inputs
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
 
 
 # --------------------------------------------------------------------------- clocks
@@ -144,7 +178,9 @@ class ClockSampler:
             self.proc.kill()
         inside = [s for t, s in self.samples if self.t0 is not None and self.t0 <= t <= self.t1 + 0.2]
         if not inside and self.samples:
-            inside = [self.samples[-1][1]]
+            # the timed region was shorter than the sampling period: the sample nearest to it
+            mid = 0.5 * (self.t0 + self.t1) if self.t0 is not None else self.samples[-1][0]
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
         names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         mhz, mx, pw = [], [], []
@@ -163,6 +199,10 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- ncu traffic record
+KERNEL_SOURCE = {"pack_weights": "pack.cu", "decode": "gemv_fused.cu", "prefill": "prefill.cu"}
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
 def source_hash(src):
     """sha256 (16 hex digits) of a kernel source and the headers every kernel includes."""
     h = hashlib.sha256()
@@ -172,46 +212,24 @@ def source_hash(src):
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel_row, workload, prefill=False):
-    """DRAM bytes per launch from the committed ncu summary of this workload, if the kernel source is unchanged."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
+def traffic_record(kind, workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if the kernel source is unchanged since the capture (else None)."""
+    path = TRAFFIC_PATH
+    if not os.path.exists(path) or kind not in KERNEL_SOURCE:
         return None
-    src = {"pack_weights": "pack.cu", "forward": "gemv_fused.cu"}[kernel_row]
-    if kernel_row == "forward" and prefill:
-        src = "prefill.cu"
-    h = source_hash(src)
+    h = source_hash(KERNEL_SOURCE[kind])
     best = None
     for line in open(path):
         parts = line.split()
-        if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == kernel_row and parts[2] == h and parts[3] == workload:
+        if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == kind and parts[2] == h and parts[3] == workload:
             best = float(parts[4])
     return best
 
 
 # --------------------------------------------------------------------------- oracle (CPU) timing
-def oracle_step(inputs, rows_per_proj, pack=True):
-    """One oracle step on the first rows_per_proj weight rows of each projection.
-    With pack=False the codes come from the set-up (packed once, reused)."""
-    import oracle
-    done = 0
-    for (w, x, p, pre) in inputs:
-        n = min(rows_per_proj, p.n)
-        if pack:
-            wn = w[:n]
-            g = oracle.absmean_gamma(wn)
-            c = oracle.ternary_codes(wn, g)
-            oracle.pack_codes(c)
-        else:
-            g, c = pre[0], pre[1][:n]
-        xq, s = oracle.quant_act(x)
-        acc = oracle.ternary_int8_matmul(xq, c)
-        oracle.rescale(acc, g, s)
-        done += n
-    return done
-
-
-def oracle_inputs(projs, pack=True):
+def _oracle_prepare(projs, pack):
+    """Per projection: (W fp32, x fp32, projection, (gamma, codes) or None)."""
     import oracle
     out = []
     for p in projs:
@@ -225,11 +243,61 @@ def oracle_inputs(projs, pack=True):
         if not pack:
             g = oracle.absmean_gamma(wn)
             pre = (g, oracle.ternary_codes(wn, g))
+            wn = None                      # only the codes are needed from here on
         out.append((wn, xf, p, pre))
     return out
 
 
-def sampled_units(projs, n_rows, unit, rows=None):
+def _oracle_part(inputs, j, r0, r1, t0, t1, pack):
+    """The oracle on weight rows [r0, r1) and tokens [t0, t1) of projection j."""
+    import oracle
+    wn, xf, p, pre = inputs[j]
+    if pack:
+        wr = wn[r0:r1]
+        g = oracle.absmean_gamma(wr)
+        c = oracle.ternary_codes(wr, g)
+        oracle.pack_codes(c)
+    else:
+        g, c = pre[0], pre[1][r0:r1]
+    xq, s = oracle.quant_act(xf[t0:t1])
+    acc = oracle.ternary_int8_matmul(xq, c)
+    oracle.rescale(acc, g, s)
+
+
+def _split(projs, n_rows, parts):
+    """Work items (projection, row range, token range) covering the first n_rows
+    rows of every projection in about `parts` pieces: by tokens when a
+    projection has many, else by rows."""
+    items = []
+    for j, p in enumerate(projs):
+        n = min(n_rows, p.n)
+        if p.m >= 64:
+            cuts = np.linspace(0, p.m, min(parts, p.m) + 1).astype(int)
+            items += [(j, 0, n, int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+        else:
+            cuts = np.linspace(0, n, min(parts, n) + 1).astype(int)
+            items += [(j, int(a), int(b), 0, p.m) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+    return items
+
+
+_POOL_INPUTS = None
+
+
+def _pool_init(names, pack):
+    global _POOL_INPUTS
+    import torch as _t
+    _t.set_num_threads(1)
+    projs = [p for name, idx in names for p in [WORKLOADS[name].projections[idx]]]
+    _POOL_INPUTS = (_oracle_prepare(projs, pack), pack)
+
+
+def _pool_task(item):
+    inputs, pack = _POOL_INPUTS
+    _oracle_part(inputs, *item, pack)
+    return 0
+
+
+def sampled_units(projs, n_rows, unit, rows):
     tot = 0
     for p in projs:
         n = min(n_rows, p.n)
@@ -238,107 +306,191 @@ def sampled_units(projs, n_rows, unit, rows=None):
     return tot
 
 
-def time_oracle(projs, unit, budget_s, steps=None, warmup=0, rows=None):
-    """Oracle throughput on a row sample sized so that `steps` steps take about budget_s.
-    rows: the bench rows the step covers (without the packing rows the codes
-    are made once before timing, as the packed-once workloads do)."""
-    pack = rows is None or "pack_weights" in rows
-    inputs = oracle_inputs(projs, pack)
-    t = time.perf_counter()
-    oracle_step(inputs, 64, pack)
-    t64 = max(time.perf_counter() - t, 1e-3)
-    n_steps = steps if steps else 1
-    n_rows = int(64 * (budget_s / n_steps) / t64)
-    n_rows = max(1, min(n_rows, max(p.n for p in projs)))
-    for _ in range(warmup):
-        oracle_step(inputs, n_rows, pack)
-    t = time.perf_counter()
-    for _ in range(n_steps):
-        oracle_step(inputs, n_rows, pack)
-    el = time.perf_counter() - t
-    units = sampled_units(projs, n_rows, unit, rows) * n_steps
-    scale = 1e9 if unit == "GB/s" else 1e12
-    return {"value": units / el / scale, "unit": unit, "cores": 1, "kind": "oracle", "seconds": el,
-            "steps": n_steps,
-            "sample": f"first {n_rows} weight rows of each of {len(projs)} projection(s) (all tokens), "
-                      f"{n_steps} step(s); numpy oracle, single thread"}
+class OracleTimer:
+    """The CPU oracle, as it stands, on a row sample of a workload: on one core
+    and on every host core (a spawned process pool over row or token ranges,
+    started before the first CUDA call)."""
+
+    def __init__(self, wl_name, projs_idx, unit, rows, cores=None):
+        self.wl = WORKLOADS[wl_name]
+        self.names = [(wl_name, i) for i in projs_idx]
+        self.projs = [self.wl.projections[i] for i in projs_idx]
+        self.unit, self.rows = unit, rows
+        self.pack = "pack_weights" in rows
+        self.host = host_cores()
+        self.cores = cores or min(self.host, MAX_ORACLE_PROCESSES)
+        self.pool = None
+        if self.cores > 1:
+            ctx = mp.get_context("spawn")
+            self.pool = ctx.Pool(self.cores, initializer=_pool_init, initargs=(self.names, self.pack))
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.terminate()
+            self.pool.join()
+
+    def _scale(self):
+        return 1e9 if self.unit == "GB/s" else 1e12
+
+    def single(self, budget_s, steps=1, warmup=0):
+        inputs = _oracle_prepare(self.projs, self.pack)
+        t = time.perf_counter()
+        for j, p in enumerate(self.projs):
+            _oracle_part(inputs, j, 0, min(64, p.n), 0, p.m, self.pack)
+        t64 = max(time.perf_counter() - t, 1e-3)
+        n_rows = max(1, min(int(64 * (budget_s / steps) / t64), max(p.n for p in self.projs)))
+        for _ in range(warmup):
+            self._run_single(inputs, n_rows)
+        t = time.perf_counter()
+        for _ in range(steps):
+            self._run_single(inputs, n_rows)
+        el = time.perf_counter() - t
+        units = sampled_units(self.projs, n_rows, self.unit, self.rows) * steps
+        return {"value": units / el / self._scale(), "unit": self.unit, "cores": 1, "kind": "oracle",
+                "seconds": el, "steps": steps,
+                "sample": f"first {n_rows} weight rows of each of {len(self.projs)} projection(s) (all tokens), "
+                          f"{steps} step(s); numpy oracle, one process"}
+
+    def _run_single(self, inputs, n_rows):
+        for j, p in enumerate(self.projs):
+            _oracle_part(inputs, j, 0, min(n_rows, p.n), 0, p.m, self.pack)
+
+    def parallel(self, budget_s, steps=1, warmup=0):
+        if self.pool is None:
+            r = self.single(budget_s, steps, warmup)
+            return r
+        # a short calibration run across the pool, then a sample sized to the budget
+        n_rows = 64 * self.cores
+        t = time.perf_counter()
+        self.pool.map(_pool_task, _split(self.projs, n_rows, self.cores), chunksize=1)
+        tc = max(time.perf_counter() - t, 1e-3)
+        n_rows = max(1, min(int(n_rows * (budget_s / steps) / tc), max(p.n for p in self.projs)))
+        items = _split(self.projs, n_rows, self.cores)
+        for _ in range(max(1, warmup)):
+            self.pool.map(_pool_task, items, chunksize=1)
+        t = time.perf_counter()
+        for _ in range(steps):
+            self.pool.map(_pool_task, items, chunksize=1)
+        el = time.perf_counter() - t
+        units = sampled_units(self.projs, n_rows, self.unit, self.rows) * steps
+        return {"value": units / el / self._scale(), "unit": self.unit, "cores": self.cores, "kind": "oracle",
+                "seconds": el, "steps": steps,
+                "sample": f"first {n_rows} weight rows of each of {len(self.projs)} projection(s) (all tokens), "
+                          f"{steps} step(s); numpy oracle, {self.cores} processes over row or token ranges "
+                          f"({self.host} host cores)"}
 
 
-# --------------------------------------------------------------------------- the GPU step
-class Step:
-    """The timed step. Single-projection workloads pack weights inside the step
-    (pack_weights, forward); the 7B-class stacks pack every layer
-    once at set-up and reuse it, so their step is the forward of every
-    projection."""
+def oracle_projection_indices(wl):
+    """The projections the oracle samples: all of a one-layer workload, one layer of a stack."""
+    return list(range(len(wl.projections) if wl.layers == 1 else len(wl.projections) // wl.layers))
 
-    def __init__(self, projs, device, rotate, pack_in_step=True):
-        import bit_ternary_forward_b300 as blt
+
+# --------------------------------------------------------------------------- the GPU sets
+def l2_bytes(device):
+    try:
+        return int(torch.cuda.get_device_properties(device).L2_cache_size) or FALLBACK_L2_BYTES
+    except Exception:
+        return FALLBACK_L2_BYTES
+
+
+def _check(lib, st):
+    if st != 0:
+        raise RuntimeError(lib.bitlinear_last_error().decode())
+
+
+class ForwardSet:
+    """Packed-once weights, activations and outputs of a list of projections in
+    `slots` distinct copies. Slot 0 holds the seeded workload (weights packed
+    by the library at set-up); further slots hold copies of its packed bytes
+    and fresh activations in their own buffers, so that rotating the slots
+    makes every forward read its packed weights from HBM."""
+
+    def __init__(self, blt, projs, device, slots):
         from workloads.synth import gaussian_activations_on, student_t_weights_on
-        self.blt = blt
-        self.lib = blt.lib
-        self.projs = projs
-        self.device = device
-        self.pack_in_step = pack_in_step
-        self.rows = ROWS if pack_in_step else ["forward"]
+        self.blt, self.lib, self.projs, self.device = blt, blt.lib, projs, device
         self.slots = []
-        for r in range(rotate):
+        for r in range(slots):
             slot = []
-            for p in projs:
-                nws = max(blt.pack_workspace_bytes(p.n, p.k), blt.forward_workspace_bytes(p.m, p.n, p.k))
-                d = {
-                    "p": p,
-                    "gamma": torch.empty(1, dtype=torch.float32, device=device),
-                    "wp": torch.empty((p.n, p.k // 4), dtype=torch.uint8, device=device),
-                    "xq": torch.empty((p.m, p.k), dtype=torch.int8, device=device),
-                    "s": torch.empty(p.m, dtype=torch.float32, device=device),
-                    "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device),
-                    "ws_t": torch.empty(nws + 256, dtype=torch.uint8, device=device),
-                    "nws": nws,
-                }
+            for j, p in enumerate(projs):
+                nws = blt.forward_workspace_bytes(p.m, p.n, p.k)
+                d = {"p": p, "y": torch.empty((p.m, p.n), dtype=torch.float32, device=device),
+                     "ws_t": torch.empty(nws + 256, dtype=torch.uint8, device=device), "nws": nws}
                 d["ws"] = (d["ws_t"].data_ptr() + 255) // 256 * 256
-                if pack_in_step:
-                    w, x = make_projection_inputs(p)
-                    d["w"] = (w.clone() if r else w).to(device)
-                    d["x"] = x.to(device)
-                else:
-                    w = student_t_weights_on(device, p.n, p.k, p.w_seed) if p.w_dist == "t4" else \
-                        make_projection_inputs(p)[0].to(device)
+                if r == 0:
+                    d["wp"] = torch.empty((p.n, p.k // 4), dtype=torch.uint8, device=device)
+                    d["gamma"] = torch.empty(1, dtype=torch.float32, device=device)
+                    if p.w_dist == "t4" and p.n * p.k > 8_000_000:
+                        w = student_t_weights_on(device, p.n, p.k, p.w_seed)
+                        x = gaussian_activations_on(device, p.m, p.k, p.x_seed)
+                    else:
+                        w, x = make_projection_inputs(p)
+                        w, x = w.to(device), x.to(device)
                     blt.pack_weights(w, out=blt.PackedWeight(d["wp"], d["gamma"], p.n, p.k))
                     torch.cuda.synchronize(device)
                     del w
-                    d["x"] = gaussian_activations_on(device, p.m, p.k, p.x_seed + 7919 * r)
+                    d["x"] = x
+                else:
+                    src = self.slots[0][j]
+                    d["wp"] = src["wp"].clone()
+                    d["gamma"] = src["gamma"].clone()
+                    d["x"] = gaussian_activations_on(device, p.m, p.k, p.x_seed + 7919 * r,
+                                                     dtype=src["x"].dtype)
                 d["xdt"] = blt.BL_BF16 if d["x"].dtype == torch.bfloat16 else blt.BL_F32
                 slot.append(d)
             self.slots.append(slot)
-        self.rotate = rotate
 
-    def run(self, i, stream, events=None):
-        """One step on rotation slot i; events receives external event records between calls."""
+    def calls(self, i):
+        """The forward calls of step i (slot i mod slots), as closures on a stream."""
         lib = self.lib
-        st = stream.cuda_stream
-        for d in self.slots[i % self.rotate]:
+        out = []
+        for d in self.slots[i % len(self.slots)]:
             p = d["p"]
-            if self.pack_in_step:
-                if events is not None:
-                    events.mark(stream)
-                self._ok(lib.bitlinear_pack_weights(d["w"].data_ptr(), p.n, p.k, d["wp"].data_ptr(),
-                                                    d["gamma"].data_ptr(), d["ws"], d["nws"], st))
-            if events is not None:
-                events.mark(stream)
-            self._ok(lib.bitlinear_forward(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(), d["gamma"].data_ptr(),
-                                           p.n, p.k, d["y"].data_ptr(), d["xq"].data_ptr(), d["s"].data_ptr(),
-                                           d["ws"], d["nws"], st))
-        if events is not None:
-            events.mark(stream)
 
-    def _ok(self, st):
-        if st != 0:
-            raise RuntimeError(self.lib.bitlinear_last_error().decode())
+            def call(st, d=d, p=p):
+                _check(lib, lib.bitlinear_forward(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(),
+                                                  d["gamma"].data_ptr(), p.n, p.k, d["y"].data_ptr(), None, None,
+                                                  d["ws"], d["nws"], st))
+            out.append((p, call))
+        return out
 
-    def launches_per_step(self):
-        return sum(len(k) for p in self.projs for r, k in row_kernels(p).items() if r in self.rows)
+    def weight_bytes_per_slot(self):
+        return sum(p.n * p.k // 4 for p in self.projs)
 
 
+class PackSet:
+    """fp32 weights of a list of projections in `slots` copies (each larger
+    than L2 in total) and their packed outputs, for timing bitlinear_pack_weights."""
+
+    def __init__(self, blt, projs, device, slots):
+        self.blt, self.lib, self.projs = blt, blt.lib, projs
+        self.slots = []
+        for r in range(slots):
+            slot = []
+            for p in projs:
+                w, _ = make_projection_inputs(p)
+                nws = blt.pack_workspace_bytes(p.n, p.k)
+                d = {"p": p, "w": w.to(device),
+                     "wp": torch.empty((p.n, p.k // 4), dtype=torch.uint8, device=device),
+                     "gamma": torch.empty(1, dtype=torch.float32, device=device),
+                     "ws_t": torch.empty(nws + 256, dtype=torch.uint8, device=device), "nws": nws}
+                d["ws"] = (d["ws_t"].data_ptr() + 255) // 256 * 256
+                slot.append(d)
+            self.slots.append(slot)
+
+    def calls(self, i):
+        lib = self.lib
+        out = []
+        for d in self.slots[i % len(self.slots)]:
+            p = d["p"]
+
+            def call(st, d=d, p=p):
+                _check(lib, lib.bitlinear_pack_weights(d["w"].data_ptr(), p.n, p.k, d["wp"].data_ptr(),
+                                                       d["gamma"].data_ptr(), d["ws"], d["nws"], st))
+            out.append((p, call))
+        return out
+
+
+# --------------------------------------------------------------------------- graphs and timing
 class GraphEvents:
     def __init__(self, pre_created):
         from cuda.bindings import runtime as rt
@@ -352,6 +504,91 @@ class GraphEvents:
         err, = self.rt.cudaEventRecordWithFlags(ev.cuda_event, stream.cuda_stream, self.rt.cudaEventRecordExternal)
         if int(err) != 0:
             raise RuntimeError(f"cudaEventRecordWithFlags failed: {err}")
+
+
+def capture(step_set, G, stream, marked=False):
+    """A CUDA graph of steps 0..G-1 of `step_set`; with marked=True an external
+    event node sits before every call and after the last (returns the events)."""
+    pool = None
+    gev = None
+    if marked:
+        n = G * len(step_set.projs) + 1
+        pool = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for ev in pool:
+            ev.record(stream)
+        stream.synchronize()
+        gev = GraphEvents(pool)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(G):
+            for _, call in step_set.calls(i):
+                if gev is not None:
+                    gev.mark(stream)
+                call(stream.cuda_stream)
+        if gev is not None:
+            gev.mark(stream)
+    g.replay()
+    stream.synchronize()
+    return g, pool
+
+
+def time_graph(graph, replays, stream, world, device, clocks=None):
+    """ms of `replays` back-to-back replays, max over ranks. A short GPU sleep
+    ahead of the start event keeps the GPU busy while the host enqueues the
+    graph, so the timed region holds the graph's own work."""
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    if clocks is not None:
+        clocks.mark("t0")
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000)
+        t_start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize(device)
+    if clocks is not None:
+        clocks.mark("t1")
+    barrier(world)
+    return max_over_ranks(t_start.elapsed_time(t_end), world, device)
+
+
+def per_call_ms(step_set, marked_graph, pool, G, stream):
+    """[(projection, ms)] of every call of one replay of the marked graph."""
+    with torch.cuda.stream(stream):
+        marked_graph.replay()
+    stream.synchronize()
+    out = []
+    k = 0
+    for i in range(G):
+        for p, _ in step_set.calls(i):
+            out.append((p, pool[k].elapsed_time(pool[k + 1])))
+            k += 1
+    return out
+
+
+def graph_steps_for(steps, cap):
+    G = max(1, min(cap, steps))
+    while steps % G:
+        G -= 1
+    return G
+
+
+def row_entry(name, timings, kind, hbm):
+    """Per-call statistics of one row from [(projection, ms)]."""
+    launches = len(timings)
+    avg_ms = sum(t for _, t in timings) / launches
+    byts = sum(row_bytes(p)[kind] for p, _ in timings) / launches
+    e = {"row": name, "kernels": sorted({k for p, _ in timings for k in row_kernels(p)[kind]}),
+         "calls": launches, "avg_us": 1e3 * avg_ms, "bytes_per_call": byts,
+         "gbs": byts / (avg_ms * 1e-3) / 1e9}
+    e["hbm_frac"] = e["gbs"] / hbm
+    if kind == "forward":
+        ops = sum(row_ops(p)["forward"] for p, _ in timings) / launches
+        e["tops"] = ops / (avg_ms * 1e-3) / 1e12
+    return e
 
 
 # --------------------------------------------------------------------------- main
@@ -384,29 +621,31 @@ def max_over_ranks(v, world, device):
     return float(t.item())
 
 
-STEP_DESC = ("pack_weights (absmean, codes, packing) + forward (act quant, contraction, rescale) per projection")
-
-
 def base_config(wl, world):
     """The config fields both arms report for a workload."""
     return {"workload": wl.name, "description": wl.description,
             "projections": [f"{p.name}: M={p.m} K={p.k} N={p.n}"
                             for p in wl.projections[:len(wl.projections) // max(wl.layers, 1)]],
             "layers": wl.layers,
-            "step": STEP_DESC if wl.layers == 1 else "forward (act quant, contraction, rescale) of every projection; "
-                                                      "weights packed once at set-up",
+            "step": "bitlinear_forward (activation quantisation, ternary x int8 contraction, rescale) of every "
+                    "projection over weights packed once at set-up",
             "parallelism": f"replicas x{world}"}
+
+
+def unit_of(wl):
+    return "GB/s" if is_decode(wl) else "TOPS"
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
     wl = WORKLOADS[args.workload]
-    projs = wl.projections if wl.layers == 1 else wl.projections[:4]
-    unit = "GB/s" if args.unit == "GB/s" else "TOPS"
-    rows = ROWS if wl.layers == 1 else ["forward"]
-    r = time_oracle(projs, unit, budget_s=args.reference_budget, steps=args.steps, warmup=min(args.warmup, 3),
-                    rows=rows)
+    unit = unit_of(wl)
+    t = OracleTimer(wl.name, oracle_projection_indices(wl), unit, ("forward",), cores=args.cpu_cores)
+    try:
+        r = t.parallel(args.reference_budget, steps=args.steps, warmup=min(args.warmup, 1))
+    finally:
+        t.close()
     line = {"metric": METRIC, "impl": "reference", "value": r["value"], "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r["seconds"] / r["steps"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f32",
@@ -419,163 +658,188 @@ def run_reference(args, world, rank):
     return 0
 
 
+def measure_forward(blt, wl, device, stream, args, world, hbm, bf16, bf16_sus, peak_src, slots, clocks=None):
+    """Whole-step throughput of the forward step of `wl` and its per-call rows."""
+    fs = ForwardSet(blt, wl.projections, device, slots)
+    unit = unit_of(wl)
+    # eager warm-up: the first use of every kernel
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            for _, call in fs.calls(i):
+                call(stream.cuda_stream)
+    stream.synchronize()
+    G = graph_steps_for(args.steps, args.graph_steps)
+    graph, _ = capture(fs, G, stream)
+    marked, pool = capture(fs, G, stream, marked=True)
+    if clocks is not None:
+        clocks.start()
+    ms = time_graph(graph, args.steps // G, stream, world, device, clocks)
+    clk = clocks.stop() if clocks is not None else None
+    per_call = per_call_ms(fs, marked, pool, G, stream)
+    scale = 1e9 if unit == "GB/s" else 1e12
+    units_step = workload_units(wl.projections, unit)
+    value = world * units_step * args.steps / (ms * 1e-3) / scale
+    row = row_entry("forward", per_call, "forward", hbm)
+    launches_per_step = sum(len(row_kernels(p)["forward"]) for p in wl.projections)
+    if unit == "GB/s":
+        # the timed step holds only forward calls: their throughput in the timed region
+        achieved = units_step * args.steps / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic_record("decode", wl.name),
+                "kernel": "forward (" + "+".join(row["kernels"]) + ")",
+                "achieved_timing": "algorithmic bytes of the timed forwards / the timed region (the step is "
+                                   "forward calls only, consecutive calls overlapping as in a decode loop)",
+                "alone": {"gbs": row["gbs"], "frac": row["gbs"] / hbm, "avg_us": row["avg_us"]},
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
+    else:
+        achieved = units_step * args.steps / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
+                "frac_of_sustained": achieved / bf16_sus, "traffic": traffic_record("prefill", wl.name),
+                "kernel": "forward (" + "+".join(row["kernels"]) + "; fp16 tcgen05.mma made exact)",
+                "achieved_timing": "2*M*N*K of the timed forwards / the timed region",
+                "alone": {"tflops": row["tops"], "frac": row["tops"] / bf16, "avg_us": row["avg_us"]},
+                "peak_source": f"MEASURED_PEAKS.json bf16_tflops burst ({peak_src}); fp16 runs at the bf16 rate"}
+    by_proj = []
+    for p in wl.projections[:len(wl.projections) // max(wl.layers, 1)]:
+        ts = [(q, t) for q, t in per_call if q.name == p.name or q.name.split(".")[-1] == p.name.split(".")[-1]]
+        e = row_entry("forward " + p.name.split(".")[-1], ts, "forward", hbm)
+        e["frac_of_bf16_burst"] = e["tops"] / bf16 if unit == "TOPS" else None
+        by_proj.append(e)
+    return {"fs": fs, "ms": ms, "value": value, "unit": unit, "units_step": units_step, "roofline": roof,
+            "row": row, "rows_by_projection": by_proj, "clocks": clk, "G": G,
+            "launches": launches_per_step * args.steps,
+            "slot_bytes": sum(4 * p.m * p.n + x_bytes(p) * p.m * p.k + p.n * p.k // 4 for p in wl.projections)}
+
+
+def measure_pack(blt, wl, device, stream, args, world, hbm):
+    """Per-call time of bitlinear_pack_weights on the workload's weights (two
+    rotating fp32 copies, each larger than L2 for the 2B shapes)."""
+    ps = PackSet(blt, wl.projections, device, 2)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            for _, call in ps.calls(i):
+                call(stream.cuda_stream)
+    stream.synchronize()
+    G = 8
+    marked, pool = capture(ps, G, stream, marked=True)
+    per_call = per_call_ms(ps, marked, pool, G, stream)
+    e = row_entry("pack_weights (one-time, outside the step)", per_call, "pack_weights", hbm)
+    e["bytes_note"] = "compulsory 4*N*K + N*K/4 + 4 (W read once); traffic = measured DRAM bytes per call"
+    e["traffic"] = traffic_record("pack_weights", wl.name)
+    del ps
+    torch.cuda.empty_cache()
+    return e
+
+
+MAX_SLOTS = 256
+
+
+def decode_slots(wl, device):
+    """Rotation slots so that the packed weights of all slots total at least 2x
+    L2 (at most MAX_SLOTS: the CPU-scale case stays in L2 and is a parity case)."""
+    wbytes = sum(p.n * p.k // 4 for p in wl.projections)
+    return max(1, min(MAX_SLOTS, math.ceil(2 * l2_bytes(device) / wbytes)))
+
+
+def prefill_slots(wl, device):
+    """Rotation slots so that each slot's activations, packed weights and outputs
+    total at least 2x L2 over all slots."""
+    b = sum(4 * p.m * p.n + x_bytes(p) * p.m * p.k + p.n * p.k // 4 for p in wl.projections)
+    return max(1, min(MAX_SLOTS, math.ceil(2 * l2_bytes(device) / b)))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="decode_2b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--graph-steps", type=int, default=250, help="steps per captured graph")
-    ap.add_argument("--rotate", type=int, default=2, help="input copies cycled between steps")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--graph-steps", type=int, default=200, help="steps per captured graph")
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--reference-budget", type=float, default=90.0)
+    ap.add_argument("--no-companions", action="store_true", help="skip the pack and prefill rows")
+    ap.add_argument("--cpu-budget", type=float, default=8.0)
+    ap.add_argument("--cpu-cores", type=int, default=0, help="processes of the all-cores oracle (0: all)")
+    ap.add_argument("--reference-budget", type=float, default=60.0)
     args = ap.parse_args(argv)
     wl = WORKLOADS[args.workload]
-    args.unit = "GB/s" if all(p.m <= 64 for p in wl.projections) else "TOPS"
 
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         return run_reference(args, world, rank)
 
+    # the all-cores oracle pool is spawned before the first CUDA call
+    timer = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        timer = OracleTimer(wl.name, oracle_projection_indices(wl), unit_of(wl), ("forward",),
+                            cores=args.cpu_cores or None)
+
+    import bit_ternary_forward_b300 as blt
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    projs = wl.projections
-    pack_in_step = wl.layers == 1
-    step = Step(projs, device, args.rotate if pack_in_step else 1, pack_in_step)
-    rows_used = step.rows
     stream = torch.cuda.Stream(device)
     hbm, bf16, bf16_sus, peak_src = peaks()
 
-    # warm-up (eager), also the first use of every kernel
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
-            step.run(i, stream)
-    stream.synchronize()
+    decode = is_decode(wl)
+    slots = decode_slots(wl, device) if decode else prefill_slots(wl, device)
+    main_res = measure_forward(blt, wl, device, stream, args, world, hbm, bf16, bf16_sus, peak_src, slots,
+                               clocks=ClockSampler(device))
+    rows = [dict(main_res["row"], row="forward (all calls of the step, each alone)")] + main_res["rows_by_projection"]
 
-    # Two graphs of G steps: the timed one holds the calls alone, so each
-    # kernel may start (programmatic dependent launch) while the one before
-    # it drains; the second has external event nodes between the calls, which
-    # end that overlap, and gives each call's own device time.
-    G = max(1, min(args.graph_steps, args.steps))
-    while args.steps % G:
-        G -= 1
-    replays = args.steps // G
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            step.run(i, stream)
-    graph.replay()
-    n_marks = G * (len(projs) * len(rows_used) + 1)
-    pool = [torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
-    for ev in pool:
-        ev.record(stream)
-    stream.synchronize()
-    gev = GraphEvents(pool)
-    marked = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(marked, stream=stream):
-        for i in range(G):
-            step.run(i, stream, events=gev)
-    marked.replay()
-    stream.synchronize()
+    e2e = run_e2e(blt, main_res["fs"], wl.projections, device, stream, args.e2e_steps, main_res["unit"])
+    del main_res["fs"]
+    torch.cuda.empty_cache()
 
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(device)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize(device)
-    clocks.mark("t0")
-    with torch.cuda.stream(stream):
-        t_start.record(stream)
-        for _ in range(replays):
-            graph.replay()
-        t_end.record(stream)
-    torch.cuda.synchronize(device)
-    clocks.mark("t1")
-    barrier(world)
-    clk = clocks.stop()
-    ms = t_start.elapsed_time(t_end)
-    ms = max_over_ranks(ms, world, device)
-
-    # per-call device times: a second timed pass over the marked graph
-    with torch.cuda.stream(stream):
-        for _ in range(min(replays, 3)):
-            marked.replay()
-    torch.cuda.synchronize(device)
-    # per-call device times from the last replay's external events
-    per_row = {r: [] for r in rows_used}
-    marks_per_step = len(projs) * len(rows_used) + 1
-    for i in range(G):
-        k = i * marks_per_step
-        for p in projs:
-            for r in rows_used:
-                per_row[r].append((p, pool[k].elapsed_time(pool[k + 1])))
-                k += 1
-    unit = args.unit
-    scale = 1e9 if unit == "GB/s" else 1e12
-    units_step = workload_units(projs, unit, rows_used)
-    value = world * units_step * args.steps / (ms * 1e-3) / scale
-
-    rows = []
-    for r in rows_used:
-        tot_ms = sum(t for _, t in per_row[r])
-        launches = len(per_row[r])
-        avg_ms = tot_ms / launches
-        byts = sum(row_bytes(p)[r] for p, _ in per_row[r]) / launches
-        gbs = byts / (avg_ms * 1e-3) / 1e9
-        kern = sorted({k for p, _ in per_row[r] for k in row_kernels(p)[r]})
-        entry = {"row": r, "kernels": kern, "avg_us": 1e3 * avg_ms, "share": None,
-                 "bytes_per_launch": byts, "gbs": gbs, "hbm_frac": gbs / hbm}
-        if r == "forward":
-            ops = sum(row_ops(p)["forward"] for p, _ in per_row[r]) / launches
-            entry["tops"] = ops / (avg_ms * 1e-3) / 1e12
-        entry["_tot"] = tot_ms
-        rows.append(entry)
-    tot_all = sum(e["_tot"] for e in rows)
-    for e in rows:
-        e["share"] = e.pop("_tot") / tot_all
-    dom = max(rows, key=lambda e: e["share"])
-    if unit == "GB/s" or dom["row"] != "forward":
-        roof = {"bound": "hbm", "achieved": dom["gbs"], "peak": hbm, "unit": "GB/s", "frac": dom["gbs"] / hbm,
-                "traffic": traffic_record(dom["row"], wl.name, unit != "GB/s"),
-                "kernel": dom["row"] + " (" + "+".join(dom["kernels"]) + ")",
-                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
-    else:
-        roof = {"bound": "tensor", "achieved": dom["tops"], "peak": bf16, "unit": "TFLOP/s",
-                "frac": dom["tops"] / bf16, "traffic": traffic_record(dom["row"], wl.name, True),
-                "kernel": dom["row"] + " (" + "+".join(dom["kernels"]) + "; fp16 tcgen05.mma, exact)",
-                "peak_source": f"MEASURED_PEAKS.json bf16_tflops burst ({peak_src}); fp16 runs at the bf16 rate",
-                "frac_of_sustained": dom["tops"] / bf16_sus}
-
-    # end to end through the public API with host buffers
-    e2e = run_e2e(step, projs, device, stream, args.e2e_steps, unit, scale)
+    companions = {}
+    if not args.no_companions and wl.layers == 1 and wl.name != "cpu_small":
+        rows.append(measure_pack(blt, wl, device, stream, args, world, hbm))
+        if decode and wl.name == "decode_2b":
+            pwl = WORKLOADS[PREFILL_COMPANION]
+            pslots = prefill_slots(pwl, device)
+            pargs = argparse.Namespace(**vars(args))
+            pargs.steps = max(10, min(args.steps, 50))
+            pre = measure_forward(blt, pwl, device, stream, pargs, world, hbm, bf16, bf16_sus, peak_src, pslots,
+                                  clocks=ClockSampler(device))
+            del pre["fs"]
+            torch.cuda.empty_cache()
+            companions["prefill"] = {
+                "workload": pwl.name, "description": pwl.description, "value": pre["value"], "unit": "TOPS",
+                "steps": pargs.steps, "ms_per_step": pre["ms"] / pargs.steps, "roofline": pre["roofline"],
+                "clocks": pre["clocks"], "slots": pslots, "gpu_launches": pre["launches"]}
+            rows += pre["rows_by_projection"]
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle(projs if pack_in_step else projs[:4], unit, budget_s=args.cpu_budget,
-                          rows=rows_used)
-        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if timer is not None:
+        try:
+            one = timer.single(args.cpu_budget)
+            allc = timer.parallel(args.cpu_budget)
+        finally:
+            timer.close()
+        cpu = {k: allc[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu["single_core"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
 
-    n_launch = step.launches_per_step() * args.steps
+    unit = main_res["unit"]
+    slot_mb = main_res["slot_bytes"] / 1e6
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "u8/i8/i32 (f32 scales)", "data": "synthetic (seeded generators)",
+        "metric": METRIC, "value": main_res["value"], "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main_res["ms"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8/i8/i32 (f32 scales)",
+        "data": "synthetic (seeded generators)",
         "config": {**base_config(wl, world),
-                   "units_per_step": units_step,
-                   "l2": f"inputs larger than L2: {args.rotate} rotating input sets of "
-                         f"{sum(4 * p.n * p.k + 2 * p.m * p.k for p in projs) / 1e6:.1f} MB",
-                   "graph_steps": G,
-                   "rows_timing": "rows and roofline from a second timed pass whose graph has event nodes "
-                                  "between the calls (each call alone, no overlap with its neighbours)"},
-        "roofline": roof,
+                   "units_per_step": main_res["units_step"],
+                   "l2": f"inputs larger than L2: {slots} rotating slot(s) of packed weights, activations and "
+                         f"outputs ({slot_mb:.1f} MB each; {slots * slot_mb:.0f} MB in all against "
+                         f"{l2_bytes(device) / 2 ** 20:.0f} MiB of L2)",
+                   "graph_steps": main_res["G"],
+                   "rows_timing": "rows from a second graph of the same calls with event nodes between them "
+                                  "(each call alone, no overlap with its neighbours)"},
+        "roofline": main_res["roofline"],
         "rows": rows,
-        "clocks": clk,
+        **companions,
+        "clocks": main_res["clocks"],
         "e2e": e2e,
-        "gpu_launches": n_launch,
+        "gpu_launches": main_res["launches"],
         "cpu_baseline": cpu,
     }
     if rank == 0:
@@ -586,31 +850,23 @@ def main(argv=None):
     return 0
 
 
-def run_e2e(step, projs, device, stream, steps, unit, scale):
-    """Host-resident inputs: H2D copies, the public API calls and a D2H of y, every step.
-
-    With packing in the step the fp32 weights are inputs too (copied and packed
-    every step); for the packed-once stacks the packed weights stay resident
-    as model state and only the activations travel."""
-    import bit_ternary_forward_b300 as blt
+def run_e2e(blt, fs, projs, device, stream, steps, unit):
+    """The step through the public Python API with host buffers: every step
+    copies each projection's activations from pinned host memory, runs
+    bit_ternary_forward_b300.forward on the resident packed weights and reads
+    y back into pinned host memory."""
+    slot = fs.slots[0]
     host = []
-    for p, d in zip(projs, step.slots[0]):
-        hx = d["x"].cpu().pin_memory()
-        hw = d["w"].cpu().pin_memory() if step.pack_in_step else None
-        host.append((p, d, hw, hx, torch.empty((p.m, p.n), dtype=torch.float32).pin_memory()))
-    dev = [(torch.empty((p.n, p.k), dtype=torch.float32, device=device) if hw is not None else None,
-            torch.empty((p.m, p.k), dtype=hx.dtype, device=device)) for p, _, hw, hx, _ in host]
-    h2d = sum((hw.numel() * 4 if hw is not None else 0) + hx.numel() * hx.element_size() for _, _, hw, hx, _ in host)
-    d2h = sum(hy.numel() * 4 for _, _, _, _, hy in host)
+    for d in slot:
+        p = d["p"]
+        host.append((d, d["x"].cpu().pin_memory(), torch.empty((p.m, p.n), dtype=torch.float32).pin_memory(),
+                     torch.empty_like(d["x"]), blt.PackedWeight(d["wp"], d["gamma"], p.n, p.k)))
+    h2d = sum(hx.numel() * hx.element_size() for _, hx, _, _, _ in host)
+    d2h = sum(hy.numel() * 4 for _, _, hy, _, _ in host)
 
     def one():
-        for (p, d, hw, hx, hy), (dw, dx) in zip(host, dev):
+        for d, hx, hy, dx, packed in host:
             dx.copy_(hx, non_blocking=True)
-            if hw is not None:
-                dw.copy_(hw, non_blocking=True)
-                packed = blt.pack_weights(dw)
-            else:
-                packed = blt.PackedWeight(d["wp"], d["gamma"], p.n, p.k)
             y = blt.forward(dx, packed)
             hy.copy_(y, non_blocking=True)
 
@@ -626,11 +882,10 @@ def run_e2e(step, projs, device, stream, steps, unit, scale):
         t1.record(stream)
     stream.synchronize()
     ms = t0.elapsed_time(t1)
-    rows = step.rows
-    return {"value": workload_units(projs, unit, rows) * steps / (ms * 1e-3) / scale, "unit": unit,
+    scale = 1e9 if unit == "GB/s" else 1e12
+    return {"value": workload_units(projs, unit) * steps / (ms * 1e-3) / scale, "unit": unit,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "api": "bit_ternary_forward_b300." + ("pack_weights + forward" if step.pack_in_step else "forward") +
-                   ", pinned host buffers"}
+            "api": "bit_ternary_forward_b300.forward on packed-once weights, x and y through pinned host buffers"}
 
 
 if __name__ == "__main__":

@@ -80,6 +80,31 @@ BL_DEVICE float rescale(int acc, float gamma, float s) {
   return __fdiv_rn(__fmul_rn(static_cast<float>(acc), gamma), s);
 }
 
+// The reciprocal div_rn_recip takes: fp32(1/s) for s inside 2^-96..2^96, and
+// 0 otherwise (such scales take the IEEE division).
+BL_DEVICE float recip_for_div(float s) { return (s > 0x1p-96f && s < 0x1p96f) ? __frcp_rn(s) : 0.f; }
+
+// fp32(t / s) rounded to nearest even, from r = recip_for_div(s), by
+// Markstein's correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q = RN(t * r), the residual e = RN(t - q * s) in one FMA, and
+// RN(q + e * r) is the correctly rounded quotient. It is taken only where
+// nothing leaves the normal range: |t| inside 2^-96..2^96 (the residual keeps
+// every bit) and |q| inside 2^-100..2^126 (a normal quotient whose correction
+// cannot overflow). A zero t gives q, which carries the sign of t / s. Every
+// other case (overflowing or underflowing quotients, scales outside
+// 2^-96..2^96) takes the IEEE division.
+BL_DEVICE float div_rn_recip(float t, float s, float r) {
+  const float q = __fmul_rn(t, r);
+  const float at = fabsf(t), aq = fabsf(q);
+  if (r != 0.f) {
+    if (t == 0.f) return q;
+    if (at > 0x1p-96f && at < 0x1p96f && aq > 0x1p-100f && aq < 0x1p126f)
+      return __fmaf_rn(__fmaf_rn(-q, s, t), r, q);
+  }
+  return __fdiv_rn(t, s);
+}
+
 // Programmatic dependent launch. Every kernel of this library runs
 //   prologue (no global reads) -> pdl_wait() -> pdl_launch_dependents() -> body
 // so a grid may become resident before its predecessor ends, no read of the

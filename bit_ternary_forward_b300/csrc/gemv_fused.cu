@@ -125,20 +125,6 @@ BL_DEVICE int sum16(const uint32_t (&w)[4]) {
   return dp4a_ss(static_cast<int>(w[3]), 0x01010101, s);
 }
 
-// fp32(t / s) rounded to nearest even from r = fp32(1/s) (r = 0: use IEEE
-// division). Markstein's correction step (P. Markstein, IBM J. Res. Dev.
-// 34(1), 1990): q = RN(t * r) is within an ulp of t/s, the residual t - q*s is
-// exact in one FMA, and q + residual * r rounded once is the correctly rounded
-// quotient, barring underflow and overflow, which the range test excludes.
-BL_DEVICE float div_by_scale(float t, float s, float r) {
-  const float at = fabsf(t);
-  if (r != 0.f && (at == 0.f || (at > 0x1p-96f && at < 0x1p96f))) {
-    const float q = __fmul_rn(t, r);
-    return __fmaf_rn(__fmaf_rn(-q, s, t), r, q);
-  }
-  return __fdiv_rn(t, s);
-}
-
 }  // namespace
 
 // ---- 1. per-token activation pass (one CTA of kActTqThreads per token)
@@ -270,7 +256,7 @@ bl_gemv_w(const uint8_t* __restrict__ wp, const uint8_t* xt, const int* rowsum, 
   for (int m = 0; m < MT; ++m) {
     rs[m] = m < M ? ld_after_wait_s32(rowsum + m) : 0;
     sc[m] = (!OUT_ACC && m < M) ? ld_after_wait_f32(scale + m) : 1.f;
-    rc[m] = (sc[m] > 0x1p-96f && sc[m] < 0x1p96f) ? __frcp_rn(sc[m]) : 0.f;
+    rc[m] = recip_for_div(sc[m]);
   }
   const float gm = OUT_ACC ? 0.f : ld_after_wait_f32(gamma);
   if (P > 1) __syncthreads();                       // s_acc cleared
@@ -328,7 +314,7 @@ bl_gemv_w(const uint8_t* __restrict__ wp, const uint8_t* xt, const int* rowsum, 
                 static_cast<int32_t*>(out)[o] = vsum[i][m] - rs[m];
               } else {
                 static_cast<float*>(out)[o] =
-                    div_by_scale(__fmul_rn(static_cast<float>(vsum[i][m] - rs[m]), gm), sc[m], rc[m]);
+                    div_rn_recip(__fmul_rn(static_cast<float>(vsum[i][m] - rs[m]), gm), sc[m], rc[m]);
               }
             }
           }
@@ -355,7 +341,7 @@ bl_gemv_w(const uint8_t* __restrict__ wp, const uint8_t* xt, const int* rowsum, 
       if constexpr (OUT_ACC) {
         static_cast<int32_t*>(out)[o] = a;
       } else {
-        static_cast<float*>(out)[o] = div_by_scale(__fmul_rn(static_cast<float>(a), gm), scm, rcm);
+        static_cast<float*>(out)[o] = div_rn_recip(__fmul_rn(static_cast<float>(a), gm), scm, rcm);
       }
     }
   }

@@ -11,7 +11,6 @@
 // device address to the ordinary packing path.
 
 #include <cstdio>
-#include <mutex>
 
 #include "bitlinear.h"
 #include "kernels.cuh"
@@ -23,35 +22,19 @@ namespace {
 constexpr size_t kScratchWords = static_cast<size_t>(bl::kMaxAbsumCtas) * bl::kPartialWords;
 __device__ __align__(256) uint32_t g_pack_scratch[kScratchWords];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
 // Device address of g_pack_scratch on the current device. In host code the
 // name g_pack_scratch is only a host-side shadow, so the address must come
-// from cudaGetSymbolAddress, once per device, with that device current.
+// from cudaGetSymbolAddress with the device current. It is looked up on every
+// call (a cheap table lookup in the runtime once the module is loaded), so no
+// address outlives a device reset and nothing is shared between host threads.
 bl_status scratch_address(void** out, const char** why) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    *why = cudaGetErrorString(e);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_pack_scratch);
+  if (e != cudaSuccess || !p) {
+    *why = e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned NULL";
     return BL_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    *why = "device ordinal out of range for the static scratch table";
-    return BL_ERR_UNSUPPORTED;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_pack_scratch);
-    if (e != cudaSuccess || !p) {
-      *why = e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned NULL";
-      return BL_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return BL_OK;
 }
 

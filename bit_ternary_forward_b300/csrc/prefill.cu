@@ -19,10 +19,11 @@
 //     stands for k = 16q + 4j + i: within each 16-code block the activations
 //     are stored transposed as a 4 x 4 matrix, matching the plane order.
 //   * Every product is then f * x_q * 2^-24 exactly, and every partial sum is
-//     an integer times 2^-24 of magnitude at most 2 * 127 * K * 2^-24 < 1 for
-//     K <= 65536, so the fp32 accumulator holds it exactly (as long as the
-//     tensor core adds integers below 2^24 without loss, which the GPU parity
-//     tests check bit for bit). The epilogue scales by 2^24,
+//     an integer times 2^-24 of magnitude at most 2 * 128 * K * 2^-24 <= 1
+//     for K <= 65536, so the fp32 accumulator holds it exactly (as long as
+//     the tensor core adds such multiples of 2^-24 without loss; the GPU
+//     parity tests drive the sum to that bound at K = 65536, on whole and on
+//     split tiles, and compare bit for bit). The epilogue scales by 2^24,
 //     subtracts the token sum of x_q (field = code + 1) and applies
 //     y = fp32(fp32(acc * gamma) / s).
 //
@@ -156,20 +157,6 @@ BL_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// fp32(t / s) rounded to nearest even, from the reciprocal r = fp32(1/s):
-// Markstein's correction step (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
-// 1990): with q = RN(t * r) within an ulp of t/s, the residual t - q*s is
-// exact in one FMA and q + residual * r, rounded once, is the correctly
-// rounded quotient. The theorem assumes no underflow or overflow, so the
-// caller takes this path only for |t| and s within 2^-96 .. 2^96 and uses
-// the IEEE division otherwise.
-BL_DEVICE float div_rn_markstein(float t, float s, float r) {
-  const float q = __fmul_rn(t, r);
-  const float e = __fmaf_rn(-q, s, t);
-  return __fmaf_rn(e, r, q);
 }
 
 }  // namespace
@@ -369,15 +356,12 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // ---- epilogue: TMEM lane = weight row, column = token.
     // D = (sum_k field * x_q) * 2^-24 exactly; every value below is an
     // integer smaller than 2^24 in magnitude, so the fp32 arithmetic is exact
-    // up to the rescale, which rounds as fp32(fp32(acc * gamma) / s).
-    // The reciprocal-and-correction division needs |t| = |acc * gamma| and s
-    // inside 2^-96..2^96: for gamma inside 2^-72..2^72 every nonzero |t| is
-    // (|acc| <= 127 * 65536), so the choice is made per 32-token chunk, which
-    // keeps the common path free of branches.
+    // up to the rescale, which rounds as fp32(fp32(acc * gamma) / s)
+    // (div_rn_recip: a reciprocal and one correction step where that is
+    // exact, the IEEE division elsewhere).
     const int et = tid - 320;                    // 0..127
     const int quarter = warp & 3;
     const float gm = OUT_ACC ? 0.f : __ldg(gamma);
-    const bool gamma_fast = OUT_ACC || (gm > 0x1p-72f && gm < 0x1p72f);
     uint32_t tcount = 0;
     for (int item = 0; item < n_items; ++item, ++tcount) {
       int tile, k0, k1;
@@ -385,21 +369,14 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
       const uint32_t b = tcount & 1u;
       float* s_scale = reinterpret_cast<float*>(misc + 256 + b * kEpiBytes);
-      float* s_rcp = s_scale + kMaxBN;           // fp32(1/s), or 0 where the IEEE division must be used
+      float* s_rcp = s_scale + kMaxBN;           // recip_for_div(s)
       float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q as (exact) fp32
-      int* s_fast = reinterpret_cast<int*>(s_rowsum + kMaxBN);   // per 32-token chunk: all reciprocals usable
       for (int i = et; i < BN; i += 128) {
         const int m = m0 + i;
         const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
         s_scale[i] = sc;
-        s_rcp[i] = (sc > 0x1p-96f && sc < 0x1p96f) ? __frcp_rn(sc) : 0.f;
-        s_rowsum[i] = static_cast<float>(m < M ? __ldg(rowsum + m) : 0);   // |sum| <= 127 K < 2^24: exact
-      }
-      for (int c = warp - 10; c < BN / 32; c += 4) {
-        const int m = m0 + c * 32 + lane;
-        const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
-        const unsigned all = __ballot_sync(0xffffffffu, OUT_ACC || (sc > 0x1p-96f && sc < 0x1p96f));
-        if (lane == 0) s_fast[c] = all == 0xffffffffu;
+        s_rcp[i] = recip_for_div(sc);
+        s_rowsum[i] = static_cast<float>(m < M ? __ldg(rowsum + m) : 0);   // |sum| <= 128 K <= 2^23: exact
       }
       named_bar(1, 128);                         // the per-token data is complete
       ok = mbar_wait_sleep(&tfull[b], (tcount >> 1) & 1u) && ok;
@@ -408,37 +385,23 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
       int32_t* arow = OUT_ACC ? static_cast<int32_t*>(out) + static_cast<size_t>(m0) * N + n : nullptr;
       // y (or acc) of tokens m0 + c0 .. m0 + c0 + 31 of row n from the sums D
+      auto put = [&](int c, float d) {
+        const float acc = __fsub_rn(__fmul_rn(d, 16777216.f), s_rowsum[c]);
+        const size_t o = static_cast<size_t>(c) * N;
+        if constexpr (OUT_ACC) {
+          arow[o] = static_cast<int>(acc);
+        } else {
+          yrow[o] = div_rn_recip(__fmul_rn(acc, gm), s_scale[c], s_rcp[c]);
+        }
+      };
       auto emit = [&](int c0, const float (&dv)[32]) {
-        const bool full_chunk = m0 + c0 + 32 <= M;
-        if (full_chunk && gamma_fast && s_fast[c0 >> 5]) {
+        if (m0 + c0 + 32 <= M) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
-            const size_t o = static_cast<size_t>(c0 + j) * N;
-            if constexpr (OUT_ACC) {
-              arow[o] = static_cast<int>(acc);
-            } else {
-              yrow[o] = div_rn_markstein(__fmul_rn(acc, gm), s_scale[c0 + j], s_rcp[c0 + j]);
-            }
-          }
+          for (int j = 0; j < 32; ++j) put(c0 + j, dv[j]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (m0 + c0 + j < M) {
-              const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
-              const size_t o = static_cast<size_t>(c0 + j) * N;
-              if constexpr (OUT_ACC) {
-                arow[o] = static_cast<int>(acc);
-              } else {
-                const float t = __fmul_rn(acc, gm);
-                const float at = fabsf(t);
-                const float rr = s_rcp[c0 + j];
-                yrow[o] = (rr != 0.f && (at == 0.f || (at > 0x1p-96f && at < 0x1p96f)))
-                              ? div_rn_markstein(t, s_scale[c0 + j], rr)
-                              : __fdiv_rn(t, s_scale[c0 + j]);
-              }
-            }
-          }
+          for (int j = 0; j < 32; ++j)
+            if (m0 + c0 + j < M) put(c0 + j, dv[j]);
         }
       };
       if (tile < sch.dp_tiles) {

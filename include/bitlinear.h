@@ -174,9 +174,11 @@ BL_API bl_status bitlinear_pack_weights_quantizer(const float* W, int64_t N, int
  * holds until the process exits. No cudaMalloc, cudaFree or other allocating
  * call is made. W, Wp and gamma are as for bitlinear_pack_weights.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture begins. Every call on a device shares the one
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress); the first call on a device may load the library's
+ * device code there, so make it before any stream capture begins. Because the
+ * address is not cached, calls after a cudaDeviceReset use the reloaded
+ * array. Every call on a device shares the one
  * array: calls whose work overlaps on the GPU (different streams, no ordering
  * between them) race and give wrong results; calls ordered on one stream are
  * safe. Nothing in the array needs to start at zero: each call writes every

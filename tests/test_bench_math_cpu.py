@@ -10,6 +10,7 @@ import os
 import sys
 from types import SimpleNamespace
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -24,13 +25,11 @@ def proj(m, k, n, x_dtype="bf16"):
 
 def test_decode_bytes_of_the_2b_projection():
     """M=1, K=2560 -> N=6912, bf16 x: packed W 4,423,680 B, x 5,120 B, y
-    27,648 B, gamma 4 B, scale 4 B (4,456,456 B), plus the x_q codes (2,560 B)
-    the forward also writes out."""
+    27,648 B, gamma 4 B and one scale 4 B: 4,456,456 B."""
     b = bench.row_bytes(proj(1, 2560, 6912))
-    assert b["forward"] == 4_423_680 + 5_120 + 27_648 + 4 + 4 + 2_560
-    # packing reads the fp32 weight twice (gamma must be complete before any
-    # code) and writes the packed bytes and gamma
-    assert b["pack_weights"] == 2 * 4 * 6912 * 2560 + 6912 * 2560 // 4 + 4
+    assert b["forward"] == 4_423_680 + 5_120 + 27_648 + 4 + 4 == 4_456_456
+    # packing: the compulsory traffic, the fp32 weight read once, packed bytes and gamma written
+    assert b["pack_weights"] == 4 * 6912 * 2560 + 6912 * 2560 // 4 + 4
 
 
 def test_fp32_activations_count_four_bytes():
@@ -45,12 +44,37 @@ def test_prefill_operations():
     assert bench.workload_units(projs, "TOPS") == 2 * 72_477_573_120
 
 
-def test_workload_units_sums_the_rows():
+def test_workload_units_sums_the_forward_bytes():
     projs = [proj(1, 2560, 6912), proj(1, 6912, 2560)]
-    total = bench.workload_units(projs, "GB/s")
-    by_row = sum(sum(bench.row_bytes(p).values()) for p in projs)
-    assert total == by_row
-    assert bench.workload_units(projs, "GB/s", rows=["forward"]) == sum(bench.row_bytes(p)["forward"] for p in projs)
+    assert bench.workload_units(projs, "GB/s") == sum(bench.row_bytes(p)["forward"] for p in projs)
+    assert bench.workload_units(projs, "GB/s", rows=("forward", "pack_weights")) == \
+        sum(sum(bench.row_bytes(p).values()) for p in projs)
+
+
+def test_rotation_covers_twice_the_l2(monkeypatch):
+    """The decode pool of packed weights is at least twice the L2 size."""
+    monkeypatch.setattr(bench, "l2_bytes", lambda device: 126 * 2 ** 20)
+    wl = bench.WORKLOADS["decode_2b"]
+    slots = bench.decode_slots(wl, None)
+    per_slot = sum(p.n * p.k // 4 for p in wl.projections)
+    assert slots * per_slot >= 2 * 126 * 2 ** 20 and (slots - 1) * per_slot < 2 * 126 * 2 ** 20
+    assert bench.decode_slots(bench.WORKLOADS["stack_7b_decode"], None) == 1     # 1.26 GB of weights
+    assert bench.prefill_slots(bench.WORKLOADS["prefill_2b"], None) >= 2
+
+
+def test_oracle_work_split_covers_the_sample_once():
+    """The all-cores oracle's work items cover every sampled row and token of
+    every projection exactly once."""
+    projs = [proj(1, 2560, 6912), proj(2048, 6912, 2560)]
+    for p, nm in zip(projs, ("a", "b")):
+        p.name = nm
+    items = bench._split(projs, 1000, 7)
+    for j, p in enumerate(projs):
+        cover = np.zeros((p.m, min(1000, p.n)), dtype=int)
+        for jj, r0, r1, t0, t1 in items:
+            if jj == j:
+                cover[t0:t1, r0:r1] += 1
+        assert (cover == 1).all()
 
 
 @pytest.mark.parametrize("m,k,want", [
@@ -105,11 +129,15 @@ def test_clock_summary_without_nvidia_smi():
     assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
 
 
-def test_traffic_record_is_keyed_to_the_kernel_source(monkeypatch):
-    got = bench.traffic_record("pack_weights", "decode_2b")
-    assert got is not None and got > 8 * 6912 * 2560 * 0.99      # W read twice, per launch
-    assert bench.traffic_record("forward", "prefill_2b", True) is not None
+def test_traffic_record_is_keyed_to_the_kernel_source(monkeypatch, tmp_path):
+    rec = tmp_path / "dram_traffic.txt"
+    h = bench.source_hash("pack.cu")
+    rec.write_text(f"# header\ntraffic pack_weights {h} decode_2b 141814400 note\n"
+                   f"traffic pack_weights 0123456789abcdef decode_2b 1 stale\n")
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(rec))
+    assert bench.traffic_record("pack_weights", "decode_2b") == 141814400
     assert bench.traffic_record("pack_weights", "no_such_workload") is None
+    assert bench.traffic_record("prefill", "decode_2b") is None
     monkeypatch.setattr(bench, "source_hash", lambda src: "0000000000000000")
     assert bench.traffic_record("pack_weights", "decode_2b") is None   # a changed kernel has no record
 

@@ -9,8 +9,9 @@ static device array inside the library instead.
 Each test calls it through the C ABI twice in a row, on different weights,
 and checks both calls against bitlinear_pack_weights given a workspace:
 packed bytes and gamma bit for bit, the tolerance the parity tests use for
-integer outputs and scales. The second call runs on whatever the first one
-left in the shared array, so it shows that nothing needs clearing.
+integer outputs and scales. Both calls are also compared with the oracle
+(gamma and packed bytes, bit for bit). The second call runs on whatever the
+first one left in the shared array, so it shows that nothing needs clearing.
 
 This file is collected last on purpose, and passes alone in a fresh process
 (where its first call also sets up the array's address) or after the rest.
@@ -24,7 +25,10 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():  # pragma: no cover - CPU runs deselect -m gpu
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
+import numpy as np  # noqa: E402
+
 import bit_ternary_forward_b300 as blt  # noqa: E402
+import oracle  # noqa: E402
 from workloads import gaussian_weights, student_t_weights  # noqa: E402
 
 
@@ -46,6 +50,10 @@ def _check_pair(weights):
         torch.cuda.synchronize()
         assert torch.equal(wp, ref.wp)
         assert torch.equal(gamma.view(torch.int32), ref.gamma.view(torch.int32))
+        wn = w.cpu().numpy()
+        g_ref = oracle.absmean_gamma(wn)
+        assert gamma.cpu().numpy().view(np.uint32)[0] == np.float32(g_ref).view(np.uint32)
+        np.testing.assert_array_equal(wp.cpu().numpy(), oracle.pack_codes(oracle.ternary_codes(wn, g_ref)))
 
 
 def test_noalloc_matches_pack_weights_decode_shapes():
