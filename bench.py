@@ -87,8 +87,11 @@ def row_ops(p):
 
 def row_kernels(p):
     """The kernels one call launches, following the library's dispatch."""
+    mt = 1 if p.m <= 1 else (2 if p.m <= 2 else 4)
     if p.k % 64 == 0 and p.m >= 17:
         fwd = ["bl_act_perm", "bl_gemm_tc"]
+    elif p.k % 64 == 0 and p.m <= 4 and mt * p.k <= 65536:
+        fwd = ["bl_gemv_dp4a"]
     elif p.k % 64 == 0 and p.m <= 4:
         fwd = ["bl_act_tq", "bl_gemv_w"]
     elif p.k % 64 == 0 and p.m <= 8:
@@ -199,7 +202,7 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- ncu traffic record
-KERNEL_SOURCE = {"pack_weights": "pack.cu", "decode": "gemv_fused.cu", "prefill": "prefill.cu"}
+KERNEL_SOURCE = {"pack_weights": "pack.cu", "decode": "gemv_dp4a.cu", "prefill": "prefill.cu"}
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 

@@ -152,7 +152,30 @@ bl_status run_tc(const void* x, int xin, const float* scale_in, const uint8_t* W
   return BL_OK;
 }
 
-// Launch plan of the fused dp4a GEMV (M <= 4); smem == 0 when it does not apply.
+// Launch plan of the one-kernel dp4a GEMV (M <= 4); smem == 0 when it does not apply.
+struct Dp4aPlan {
+  int rows = 0;
+  size_t smem = 0;
+};
+
+Dp4aPlan dp4a_plan(int64_t M, int64_t N, int64_t K) {
+  Dp4aPlan p;
+  if (M > bl::kGemvDp4aMaxM) return p;
+  p.smem = bl::gemv_dp4a_plan(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), sm_count(), &p.rows);
+  return p;
+}
+
+bl_status launch_dp4a(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma, void* out,
+                      bool out_acc, int8_t* xq_out, float* scale_out, int64_t M, int64_t N, int64_t K,
+                      const Dp4aPlan& p, cudaStream_t s) {
+  cudaError_t e = bl::launch_gemv_dp4a(wp, x, xin, scale_in, gamma, out, out_acc, xq_out, scale_out,
+                                       static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), p.rows, p.smem, s);
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemv_dp4a: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
+// Launch plan of the two-kernel dp4a GEMV (M <= 4, shapes the one-kernel form
+// does not take); smem == 0 when it does not apply.
 struct GemvPlan {
   int rows = 0, parts = 0;
   size_t smem = 0;
@@ -203,13 +226,14 @@ int bitlinear_version(void) { return 1; }
 bl_status bitlinear_device_error(int* flag) {
   g_last_error.clear();
   if (!flag) return fail(BL_ERR_INVALID_ARG, "null pointer (flag)");
-  int a = 0, b = 0, c = 0, d = 0;
+  int a = 0, b = 0, c = 0, d = 0, f = 0;
   cudaError_t e = bl::take_wait_error(&a);
   if (e == cudaSuccess) e = bl::take_gemv_wait_error(&b);
   if (e == cudaSuccess) e = bl::take_tc_wait_error(&c);
   if (e == cudaSuccess) e = bl::take_pack_wait_error(&d);
+  if (e == cudaSuccess) e = bl::take_dp4a_wait_error(&f);
   if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bitlinear_device_error: %s", cudaGetErrorString(e));
-  *flag = a | b | c | d;
+  *flag = a | b | c | d | f;
   return BL_OK;
 }
 
@@ -393,6 +417,7 @@ bl_status bitlinear_quant_act(const void* x, bl_dtype dt, int64_t M, int64_t K, 
 size_t bitlinear_forward_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (use_tc(M, K)) return tc_workspace_bytes(M, N, K);
+  if (dp4a_plan(M, N, K).smem) return 0;
   return small_workspace_bytes(M, K);
 }
 
@@ -417,6 +442,8 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
                         : reinterpret_cast<float*>(ws + align_up(static_cast<size_t>(M) * static_cast<size_t>(K), 256));
   const int xin = dt == BL_BF16 ? bl::kXinBF16 : bl::kXinF32;
   if (use_tc(M, K)) return run_tc(x, xin, nullptr, Wp, gamma, y, false, xq_out, scale_out, M, N, K, workspace, s);
+  const Dp4aPlan dp = dp4a_plan(M, N, K);
+  if (dp.smem) return launch_dp4a(Wp, x, xin, nullptr, gamma, y, false, xq_out, scale_out, M, N, K, dp, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem)
     return launch_gemv_fused(Wp, x, xin, nullptr, gamma, y, false, xq_out, scale_out, M, N, K, gp, workspace, s);
@@ -432,6 +459,7 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
 size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (use_tc(M, K)) return tc_workspace_bytes(M, N, K);
+  if (dp4a_plan(M, N, K).smem) return 0;
   if (gemv_plan(M, N, K).smem) return small_workspace_bytes(M, K);
   return 0;
 }
@@ -448,6 +476,8 @@ bl_status bitlinear_gemm(const int8_t* xq, const float* scale, int64_t M, const 
     return fail(BL_ERR_WORKSPACE, "gemm workspace needs %zu bytes, 256-byte aligned", need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc(M, K)) return run_tc(xq, bl::kXinI8, scale, Wp, gamma, y, false, nullptr, nullptr, M, N, K, workspace, s);
+  const Dp4aPlan dp = dp4a_plan(M, N, K);
+  if (dp.smem) return launch_dp4a(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, dp, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, scale, gamma, y, false, nullptr, nullptr, M, N, K, gp, workspace, s);
   if (const int rows = decode_rows(N, K))
@@ -471,6 +501,8 @@ bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp, int64_t M, int
     return fail(BL_ERR_WORKSPACE, "gemm_i32 workspace needs %zu bytes, 256-byte aligned", need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (use_tc(M, K)) return run_tc(xq, bl::kXinI8, nullptr, Wp, nullptr, acc, true, nullptr, nullptr, M, N, K, workspace, s);
+  const Dp4aPlan dp = dp4a_plan(M, N, K);
+  if (dp.smem) return launch_dp4a(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, dp, s);
   const GemvPlan gp = gemv_plan(M, N, K);
   if (gp.smem) return launch_gemv_fused(Wp, xq, bl::kXinI8, nullptr, nullptr, acc, true, nullptr, nullptr, M, N, K, gp, workspace, s);
   if (const int rows = decode_rows(N, K))

@@ -87,6 +87,21 @@ BL_DEVICE void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_
       : "memory");
 }
 
+// Moves `bytes` (a multiple of 16, 16-byte aligned source) of global memory
+// into L2 ahead of use. A prefetch returns no data and L2 is the point of
+// coherence, so it cannot change what a later load sees: a kernel may issue it
+// before its dependency wait, while the kernel before it is still writing.
+BL_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// L2 prefetches of [p, p + bytes) in pieces of at most 32 KB.
+BL_DEVICE void prefetch_l2_range(const void* p, uint64_t bytes) {
+  const uint8_t* b = static_cast<const uint8_t*>(p);
+  for (uint64_t off = 0; off < bytes; off += 32768)
+    prefetch_l2(b + off, static_cast<uint32_t>(bytes - off < 32768 ? bytes - off : 32768));
+}
+
 // L2 eviction-priority policies for cache-hinted copies.
 BL_DEVICE uint64_t l2_evict_last() {
   uint64_t p;

@@ -94,6 +94,10 @@ BL_DEVICE float recip_for_div(float s) { return (s > 0x1p-96f && s < 0x1p96f) ? 
 // cannot overflow). A zero t gives q, which carries the sign of t / s. Every
 // other case (overflowing or underflowing quotients, scales outside
 // 2^-96..2^96) takes the IEEE division.
+// The IEEE division out of line, so that the unrolled loops that may need it
+// keep their code small.
+static __device__ __noinline__ float div_ieee(float t, float s) { return __fdiv_rn(t, s); }
+
 BL_DEVICE float div_rn_recip(float t, float s, float r) {
   const float q = __fmul_rn(t, r);
   const float at = fabsf(t), aq = fabsf(q);
@@ -102,7 +106,7 @@ BL_DEVICE float div_rn_recip(float t, float s, float r) {
     if (at > 0x1p-96f && at < 0x1p96f && aq > 0x1p-100f && aq < 0x1p126f)
       return __fmaf_rn(__fmaf_rn(-q, s, t), r, q);
   }
-  return __fdiv_rn(t, s);
+  return div_ieee(t, s);
 }
 
 // Programmatic dependent launch. Every kernel of this library runs

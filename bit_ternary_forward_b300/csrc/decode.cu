@@ -9,7 +9,9 @@
 // forward-pass sentence (multiply back by the factors).
 //
 // Work split. Each CTA owns a contiguous block of weight rows [n0, n0 + R).
-// One thread copies the block into shared memory with one bulk async copy
+// Before its dependency wait, thread 0 prefetches the block into L2 (a hint
+// that cannot change what later loads see). After the wait,
+// one thread copies the block into shared memory with one bulk async copy
 // per row (rows padded by 16 bytes so that the MMA fragment loads are free of
 // bank conflicts), one mbarrier per 16-row tile; meanwhile all threads
 // quantise (or stage) the activations of up to 8 tokens. The contraction
@@ -129,6 +131,8 @@ bl_decode_mma(const uint8_t* __restrict__ wp, const void* __restrict__ x, const 
   float* s_red = s_scale + kTok;
   uint64_t* s_bar = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(s_red + kWarps * kTok) + 7) & ~uintptr_t(7));
 
+  // the block's packed rows start moving into L2 while the previous kernel ends
+  if (tid == 0) prefetch_l2_range(wp + static_cast<size_t>(n0) * rowbytes, static_cast<uint64_t>(R) * rowbytes);
   pdl_wait();
   pdl_launch_dependents();
   x = launder(x);
@@ -332,22 +336,11 @@ size_t decode_smem_bytes(int rows_per_cta, int K) {
   return b < kOneCtaPerSmSmem ? kOneCtaPerSmSmem : b;
 }
 
-// One attribute call per kernel instance and size, not per launch.
-template <int XIN, bool OUT_ACC>
-cudaError_t set_smem(size_t smem) {
-  static size_t done = 0;   // one cache per template instance
-  if (smem <= done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(bl_decode_mma<XIN, OUT_ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e == cudaSuccess) done = smem;
-  return e;
-}
-
 template <int XIN, bool OUT_ACC>
 cudaError_t launch_decode_t(const uint8_t* wp, const void* x, const float* scale_in, const float* gamma, void* out,
                             int8_t* xq_out, float* scale_out, int M, int N, int K, int rows_per_cta, cudaStream_t s) {
   const size_t smem = decode_smem_bytes(rows_per_cta, K);
-  cudaError_t e = set_smem<XIN, OUT_ACC>(smem);
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(bl_decode_mma<XIN, OUT_ACC>), smem);
   if (e != cudaSuccess) return e;
   const int grid = (N + rows_per_cta - 1) / rows_per_cta;
   return launch_pdl(bl_decode_mma<XIN, OUT_ACC>, dim3(grid), dim3(kDecodeThreads), smem, s, wp, x, scale_in, gamma,

@@ -171,10 +171,8 @@ cudaError_t launch_gemv(const uint8_t* wp, const int8_t* xq, const float* scale,
 #undef BL_PICK
   const int Kp = (K + 63) & ~63;
   const size_t smem = static_cast<size_t>(mt) * Kp;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  const cudaError_t e = ensure_smem(reinterpret_cast<const void*>(fn), smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(grid_x, (M + mt - 1) / mt);
   return launch_pdl(fn, grid, dim3(kGemvThreads), smem, s, wp, xq, scale, gamma, out, M, N, K);
 }

@@ -28,6 +28,13 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Records `msg` as the calling thread's last error and returns `st` (abi.cu).
 bl_status record_error(bl_status st, const char* msg);
 
+// Per-device kernel set-up (setup.cu), thread-safe: raise `func`'s dynamic
+// shared-memory limit on the current device to at least `bytes` (a no-op up
+// to the default 48 KB), and the resident CTAs per SM of `func` with
+// `threads` threads and `bytes` of dynamic shared memory (0 if it cannot run).
+cudaError_t ensure_smem(const void* func, size_t bytes);
+int resident_ctas(const void* func, int threads, size_t bytes);
+
 // ---- weight packing (pack.cu)
 // Both weight-pass kernels stream W through a ring of shared-memory stages
 // filled by bulk copies: consumer threads plus one producer warp.
@@ -114,6 +121,23 @@ cudaError_t launch_gemv_fused(const uint8_t* wp, const void* x, int xin, const f
                               void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K,
                               int rows_per_cta, int parts, size_t smem, void* workspace, cudaStream_t s);
 cudaError_t take_gemv_wait_error(int* flag);
+
+// ---- decode GEMV for M <= 4 in one kernel: activation pass + dp4a contraction (gemv_dp4a.cu)
+constexpr int kGemvDp4aThreads = 512;
+constexpr int kGemvDp4aMaxM = 4;
+constexpr size_t kGemvDp4aMaxAct = 65536;          // bytes of quantised activations (tokens rounded to 1, 2, 4) x K
+constexpr size_t kGemvDp4aMaxSmem = 110 * 1024;    // two CTAs fit on an SM: this one and the next kernel's
+// Rows of W per CTA for M x N x K on `sms` SMs; returns the dynamic shared
+// memory in bytes, or 0 if the kernel does not take the shape (M > 4,
+// K % 64 != 0, or the activations do not fit).
+size_t gemv_dp4a_plan(int M, int N, int K, int sms, int* rows_per_cta);
+// x is fp32 / bf16 (quantised in the kernel; xq_out and scale_out optional) or
+// int8 x_q with scale_in (xin == kXinI8). out is fp32 y or int32 acc (out_acc,
+// int8 input only). No workspace.
+cudaError_t launch_gemv_dp4a(const uint8_t* wp, const void* x, int xin, const float* scale_in, const float* gamma,
+                             void* out, bool out_acc, int8_t* xq_out, float* scale_out, int M, int N, int K,
+                             int rows_per_cta, size_t smem, cudaStream_t s);
+cudaError_t take_dp4a_wait_error(int* flag);
 
 // ---- prefill contraction on tcgen05 (prefill.cu)
 constexpr int kTcMinM = 17;   // smallest M routed to the tensor-core kernel (below it the

@@ -543,18 +543,8 @@ cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, const float* g
                               cudaStream_t s) {
   const bool fused = partials != nullptr;
   auto kern = fused ? bl_quant_pack<true> : bl_quant_pack<false>;
-  // resident CTAs per SM of each form (0: the shared memory cannot be reserved)
-  auto per_sm_of = [](const void* k) {
-    int n = 0;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRingSmem)) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kPackThreads + 32, kRingSmem) != cudaSuccess)
-      n = 0;
-    return n;
-  };
-  static const int per_sm_plain = per_sm_of(reinterpret_cast<const void*>(bl_quant_pack<false>));
-  static const int per_sm_fused = per_sm_of(reinterpret_cast<const void*>(bl_quant_pack<true>));
-  const int per_sm = fused ? per_sm_fused : per_sm_plain;
+  // resident CTAs per SM (0: the shared memory cannot be reserved)
+  const int per_sm = resident_ctas(reinterpret_cast<const void*>(kern), kPackThreads + 32, kRingSmem);
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
   const uint64_t n_words = n_bytes / 4;
   const uint64_t stages = (n_words + kRingStageF4 / 4 - 1) / (kRingStageF4 / 4);
@@ -566,17 +556,9 @@ cudaError_t launch_quant_pack(const float4* w4, uint64_t n_bytes, const float* g
 }
 
 int absum_ctas_per_sm(bool masked) {
-  auto per_sm_of = [](const void* k) {
-    int n = 0;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRingSmem)) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kAbsumThreads + 32, kRingSmem) != cudaSuccess)
-      n = 0;
-    return n;
-  };
-  static const int plain = per_sm_of(reinterpret_cast<const void*>(bl_absum_partials<false>));
-  static const int masked_n = per_sm_of(reinterpret_cast<const void*>(bl_absum_partials<true>));
-  return masked ? masked_n : plain;
+  const void* k = masked ? reinterpret_cast<const void*>(bl_absum_partials<true>)
+                         : reinterpret_cast<const void*>(bl_absum_partials<false>);
+  return resident_ctas(k, kAbsumThreads + 32, kRingSmem);
 }
 
 cudaError_t launch_absum(const float4* w4, uint64_t n4, uint32_t* partials, const float* mask_gamma, float factor,

@@ -74,6 +74,7 @@ constexpr int kEStages = 3;                 // expanded-weight ring
 constexpr int kThreads = 448;
 constexpr int kMaxBN = 256;                 // tokens per tile at most: the MMA's N
 constexpr int kMaxStages = 10;
+constexpr int kPrefetchStages = 32;         // weight boxes a CTA prefetches into L2 before its dependency wait
 constexpr uint32_t kTmemCols = 512;         // two accumulators of up to 256 columns
 constexpr uint32_t kWpBytes = kBM * kBK / 4;    // 2048
 constexpr uint32_t kWeBytes = kBM * kBK * 2;    // 16384
@@ -96,6 +97,13 @@ constexpr uint32_t smem_for(int bn) {
   return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + kEStages * kWeBytes + kMiscBytes + 1024;
 }
 __device__ int g_tc_wait_error;
+
+// L2 prefetch of one box of a tensor map.
+BL_DEVICE void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
 
 BL_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
@@ -266,6 +274,18 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The packed weights of this CTA's first k-stages start moving into L2
+  // while the grid before ends (a prefetch cannot change what later loads
+  // see); the activation operand is written by that grid, so it waits.
+  if (warp == 0 && lane == 0) {
+    int done = 0;
+    for (int item = 0; item < n_items && done < kPrefetchStages; ++item) {
+      int tile, k0, k1;
+      sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
+      const int n0 = (tile % n_tiles_n) * kBM;
+      for (int it = k0; it < k1 && done < kPrefetchStages; ++it, ++done) tma_prefetch_2d(&tm_w, it * (kBK / 4), n0);
+    }
+  }
   pdl_wait();                                    // inputs come from the grid before (TMA reads after this)
   pdl_launch_dependents();
   scale = launder(scale);
@@ -356,12 +376,19 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // ---- epilogue: TMEM lane = weight row, column = token.
     // D = (sum_k field * x_q) * 2^-24 exactly; every value below is an
     // integer smaller than 2^24 in magnitude, so the fp32 arithmetic is exact
-    // up to the rescale, which rounds as fp32(fp32(acc * gamma) / s)
-    // (div_rn_recip: a reciprocal and one correction step where that is
-    // exact, the IEEE division elsewhere).
+    // up to the rescale, which rounds as fp32(fp32(acc * gamma) / s).
+    // The reciprocal-and-correction division is exact when t = acc * gamma
+    // and the quotient stay in the normal range. With gamma inside
+    // 2^-72..2^72, every nonzero |t| lies in gamma..2^24 gamma, inside
+    // 2^-96..2^96, and a zero t (acc = 0, so t = +0) gives +0 either way; so a
+    // 32-token chunk takes the branch-free form when every scale lies in
+    // 2^-96..2^96 and 2^24 gamma max(1/s) < 2^125 and gamma min(1/s) > 2^-99
+    // (no quotient can leave the normal range). Other chunks take
+    // div_rn_recip, which checks each output.
     const int et = tid - 320;                    // 0..127
     const int quarter = warp & 3;
     const float gm = OUT_ACC ? 0.f : __ldg(gamma);
+    const bool gamma_fast = OUT_ACC || (gm > 0x1p-72f && gm < 0x1p72f);
     uint32_t tcount = 0;
     for (int item = 0; item < n_items; ++item, ++tcount) {
       int tile, k0, k1;
@@ -369,14 +396,29 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
       const uint32_t b = tcount & 1u;
       float* s_scale = reinterpret_cast<float*>(misc + 256 + b * kEpiBytes);
-      float* s_rcp = s_scale + kMaxBN;           // recip_for_div(s)
+      float* s_rcp = s_scale + kMaxBN;           // recip_for_div(s): fp32(1/s), or 0 outside 2^-96..2^96
       float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q as (exact) fp32
+      int* s_fast = reinterpret_cast<int*>(s_rowsum + kMaxBN);   // per 32-token chunk: the branch-free form is exact
       for (int i = et; i < BN; i += 128) {
         const int m = m0 + i;
         const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
         s_scale[i] = sc;
         s_rcp[i] = recip_for_div(sc);
         s_rowsum[i] = static_cast<float>(m < M ? __ldg(rowsum + m) : 0);   // |sum| <= 128 K <= 2^23: exact
+      }
+      for (int c = warp - 10; c < BN / 32; c += 4) {
+        const int m = m0 + c * 32 + lane;
+        const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
+        const float r = recip_for_div(sc);
+        float rmax = r, rmin = r;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          rmax = fmaxf(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+          rmin = fminf(rmin, __shfl_xor_sync(0xffffffffu, rmin, o));
+        }
+        const bool fast = OUT_ACC || (gamma_fast && rmin != 0.f && __fmul_rn(__fmul_rn(gm, 0x1p24f), rmax) < 0x1p125f &&
+                                      __fmul_rn(gm, rmin) > 0x1p-99f);
+        if (lane == 0) s_fast[c] = fast;
       }
       named_bar(1, 128);                         // the per-token data is complete
       ok = mbar_wait_sleep(&tfull[b], (tcount >> 1) & 1u) && ok;
@@ -385,23 +427,35 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
       int32_t* arow = OUT_ACC ? static_cast<int32_t*>(out) + static_cast<size_t>(m0) * N + n : nullptr;
       // y (or acc) of tokens m0 + c0 .. m0 + c0 + 31 of row n from the sums D
-      auto put = [&](int c, float d) {
-        const float acc = __fsub_rn(__fmul_rn(d, 16777216.f), s_rowsum[c]);
-        const size_t o = static_cast<size_t>(c) * N;
-        if constexpr (OUT_ACC) {
-          arow[o] = static_cast<int>(acc);
-        } else {
-          yrow[o] = div_rn_recip(__fmul_rn(acc, gm), s_scale[c], s_rcp[c]);
-        }
-      };
       auto emit = [&](int c0, const float (&dv)[32]) {
-        if (m0 + c0 + 32 <= M) {
+        const bool full_chunk = m0 + c0 + 32 <= M;
+        if (full_chunk && s_fast[c0 >> 5]) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) put(c0 + j, dv[j]);
+          for (int j = 0; j < 32; ++j) {
+            const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
+            const size_t o = static_cast<size_t>(c0 + j) * N;
+            if constexpr (OUT_ACC) {
+              arow[o] = static_cast<int>(acc);
+            } else {
+              const float t = __fmul_rn(acc, gm);
+              const float r = s_rcp[c0 + j];
+              const float q = __fmul_rn(t, r);
+              yrow[o] = __fmaf_rn(__fmaf_rn(-q, s_scale[c0 + j], t), r, q);
+            }
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (m0 + c0 + j < M) put(c0 + j, dv[j]);
+          for (int j = 0; j < 32; ++j) {
+            if (m0 + c0 + j < M) {
+              const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
+              const size_t o = static_cast<size_t>(c0 + j) * N;
+              if constexpr (OUT_ACC) {
+                arow[o] = static_cast<int>(acc);
+              } else {
+                yrow[o] = div_rn_recip(__fmul_rn(acc, gm), s_scale[c0 + j], s_rcp[c0 + j]);
+              }
+            }
+          }
         }
       };
       if (tile < sch.dp_tiles) {
@@ -750,16 +804,11 @@ template <int BN, bool OUT_ACC>
 cudaError_t launch_tc_t(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const float* scale, const int* rowsum,
                         const float* gamma, void* out, int M, int N, int K, const TcPlan& p, void* sk_ws,
                         cudaStream_t s) {
-  static size_t done = 0;
   constexpr size_t smem = smem_for(BN);
   static_assert(smem <= kSmemBudget, "shared memory budget");
   static_assert(stages_for(BN) >= 4, "pipeline depth");
-  if (done < smem) {
-    cudaError_t e = cudaFuncSetAttribute(bl_gemm_tc<BN, OUT_ACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    done = smem;
-  }
+  const cudaError_t e = ensure_smem(reinterpret_cast<const void*>(bl_gemm_tc<BN, OUT_ACC>), smem);
+  if (e != cudaSuccess) return e;
   const TcSched sch = sched_of(p);
   float* sk_buf = static_cast<float*>(sk_ws);
   int* sk_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(sk_ws) + p.sk_buf_bytes);

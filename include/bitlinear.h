@@ -49,11 +49,11 @@
  *   - x, W, Wp, x_q and y must be 16-byte aligned. M, N, K > 0, K % 4 == 0,
  *     N * K < 2^32 and K <= 65536 (the int32 accumulator of |acc| <= 127*K).
  *   - Inputs must be finite; NaN or Inf inputs give unspecified codes.
- *   - Several host threads may call the library on one device; the last
- *     error message is thread-local. Each kernel's shared-memory limit is
- *     raised once per process, on the device current at its first launch, so
- *     one process should drive one GPU (a second device's launches of those
- *     kernels fail with BL_ERR_CUDA rather than run).
+ *   - Several host threads may call the library, on one device or on
+ *     several; the last error message is thread-local. Each kernel's
+ *     shared-memory limit is raised once per (device, kernel), on the device
+ *     current in the calling thread, in a table guarded by a mutex, so first
+ *     calls may happen concurrently and one process may drive several GPUs.
  */
 #ifndef BITLINEAR_H
 #define BITLINEAR_H

@@ -58,7 +58,11 @@ def test_constants(blt):
     assert lib.bitlinear_strerror(0) == b"ok"
     assert b"invalid" in lib.bitlinear_strerror(1)
     assert lib.bitlinear_pack_workspace_bytes(6912, 2560) >= 64 * 148
-    assert lib.bitlinear_forward_workspace_bytes(4, 256, 256) >= 4 * 256
+    # the one-kernel decode GEMV (M <= 4, K % 64 == 0) needs no workspace; the
+    # two-kernel forms keep the codes there
+    assert lib.bitlinear_forward_workspace_bytes(4, 256, 256) == 0
+    assert lib.bitlinear_forward_workspace_bytes(4, 256, 260) >= 4 * 260
+    assert lib.bitlinear_forward_workspace_bytes(8, 256, 256) >= 8 * 256
     assert lib.bitlinear_forward_workspace_bytes(0, 256, 256) == 0
 
 
@@ -104,7 +108,9 @@ def test_forward_and_quant_reject_bad_args_on_host(blt):
     assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 62, 16, None, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
     assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 64, 24, None, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
     assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 64, 16, 8, None, 256, ws, None) == blt.BL_ERR_INVALID_ARG
-    assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 64, 16, None, None, None, ws, None) == blt.BL_ERR_WORKSPACE
+    ws68 = lib.bitlinear_forward_workspace_bytes(4, 64, 68)     # K % 64 != 0: the two-kernel path keeps codes there
+    assert ws68 > 0
+    assert lib.bitlinear_forward(16, 1, 4, 16, 16, 64, 68, 16, None, None, None, ws68, None) == blt.BL_ERR_WORKSPACE
     assert lib.bitlinear_quant_act(16, 1, 4, 6, 16, 16, None) == blt.BL_ERR_INVALID_ARG
     assert lib.bitlinear_quant_act(None, 1, 4, 8, 16, 16, None) == blt.BL_ERR_INVALID_ARG
     assert lib.bitlinear_gemm_i32(16, 16, 4, 4, 6, 16, None, 0, None) == blt.BL_ERR_INVALID_ARG

@@ -78,7 +78,7 @@ def test_oracle_work_split_covers_the_sample_once():
 
 
 @pytest.mark.parametrize("m,k,want", [
-    (1, 2560, ["bl_act_tq", "bl_gemv_w"]), (4, 2560, ["bl_act_tq", "bl_gemv_w"]),
+    (1, 2560, ["bl_gemv_dp4a"]), (4, 2560, ["bl_gemv_dp4a"]), (4, 32768, ["bl_act_tq", "bl_gemv_w"]),
     (8, 2560, ["bl_decode_mma"]), (16, 2560, ["bl_act_quant", "bl_decode_mma"]),
     (17, 2560, ["bl_act_perm", "bl_gemm_tc"]), (2048, 6912, ["bl_act_perm", "bl_gemm_tc"]),
 ])

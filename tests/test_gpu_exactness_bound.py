@@ -177,7 +177,7 @@ def test_gaussian_forward_k65536_tensor_core():
 @pytest.mark.parametrize("m", [1, 4, 24])
 def test_rescale_overflow_and_underflow(m):
     """y = fp32(fp32(acc * gamma) / s) where the quotient overflows to +-inf
-    (activations near 1e30, gamma near 1e6) or lands far below the normal
+    (activations near 1e30, gamma 1e9) or lands far below the normal
     range (tiny gamma, tiny activations' reciprocal scale), through the
     forward's own epilogue: M = 1 and 4 on the dp4a GEMV, M = 24 on the
     tensor-core path."""
@@ -186,9 +186,10 @@ def test_rescale_overflow_and_underflow(m):
     codes = rng.integers(-1, 2, size=(n, k)).astype(np.int8)
     wp = torch.from_numpy(oracle.pack_codes(codes)).cuda()
     cases = []
-    # huge activations (s ~ 1.3e-28) with gamma ~ 1e6: t / s overflows
+    # huge activations (s ~ 4e-29, inside the fast division's scale range)
+    # with gamma 1e9: t / s overflows to +-inf for most outputs
     xa = (rng.standard_normal((m, k)) * 1e30).astype(np.float32)
-    cases.append((xa, np.float32(1.0e6)))
+    cases.append((xa, np.float32(1.0e9)))
     # tiny gamma with unit activations: t / s far below 2^-100 (subnormal or zero)
     xb = rng.standard_normal((m, k)).astype(np.float32)
     cases.append((xb, np.float32(1.0e-38)))
@@ -215,10 +216,10 @@ def test_rescale_overflow_reaches_infinity():
     x = (rng.standard_normal((m, k)) * 1e30).astype(np.float32)
     xq_ref, s_ref = oracle.quant_act(x)
     with np.errstate(over="ignore"):
-        y_ref = oracle.rescale(oracle.ternary_int8_matmul(xq_ref, codes), np.float32(1.0e6), s_ref)
+        y_ref = oracle.rescale(oracle.ternary_int8_matmul(xq_ref, codes), np.float32(1.0e9), s_ref)
     assert np.isinf(y_ref).sum() > 0
     packed = blt.PackedWeight(torch.from_numpy(oracle.pack_codes(codes)).cuda(),
-                              torch.tensor([np.float32(1.0e6)]).cuda(), n, k)
+                              torch.tensor([np.float32(1.0e9)]).cuda(), n, k)
     y = blt.forward(torch.from_numpy(x).cuda(), packed)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bits(y.cpu().numpy()), bits(y_ref))

@@ -67,10 +67,39 @@ def test_stack_7b_last_layer_prefill_sampled(proj):
     compare_sampled_rows(w, x, rows)
 
 
+# ------------------------------------------------------------------ chained calls (dependent launch)
+@pytest.mark.parametrize("m", [1, 3, 8, 24])
+def test_chained_forwards_against_the_oracle_chain(m):
+    """Forwards back to back on one stream, each reading the fp32 output of
+    the one before as its input, with every weight packed on the same stream
+    just before its forward (so a forward's weights are written by the kernel
+    it follows). Every kernel is a programmatic dependent launch; the chain
+    must match the oracle's chain output by output, bit for bit."""
+    dims = [2560, 6912, 2560, 4096, 1088, 256]
+    ws = [gaussian_weights(dims[i + 1], dims[i], seed=700 + i) for i in range(len(dims) - 1)]
+    x0 = gaussian_activations(m, dims[0], seed=800 + m, dtype=torch.float32)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        wd = [w.cuda() for w in ws]
+        x = x0.cuda()
+        for w in wd:
+            packed = blt.pack_weights(w)
+            x = blt.forward(x, packed)
+            outs.append(x)
+    s.synchronize()
+    ref = x_to_oracle(x0)
+    for i, (w, y) in enumerate(zip(ws, outs)):
+        r = oracle.bitlinear_forward(ref, w.numpy())
+        np.testing.assert_array_equal(bits(y.cpu().numpy()), bits(r["y"]), err_msg=f"projection {i}")
+        ref = r["y"]
+
+
 # ------------------------------------------------------------------ shapes and tails
 @pytest.mark.parametrize("m,n,k", [
     (1, 1, 4), (1, 3, 8), (2, 5, 12), (3, 7, 100), (5, 9, 64), (4, 33, 192), (2, 17, 1028),
     (7, 65, 320), (9, 31, 4096), (1, 130, 65536), (4, 64, 65536), (17, 129, 960), (64, 300, 2560),
+    (3, 200, 16384), (2, 77, 32768), (1, 4096, 11008), (2, 1000, 64),
     (65, 257, 128), (129, 96, 1088), (33, 70, 100), (17, 9, 1028),
 ])
 @pytest.mark.parametrize("xdt", [torch.bfloat16, torch.float32])
