@@ -213,11 +213,12 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
   // ---- activations: scale, codes, token sums, transposed blocks in shared memory
   const uint32_t s_act32 = smem_u32(s_act);
   const int total = M * nw;                      // words over all tokens
-  float sc[MT];
+  float sc[MT], rc[MT];                          // scales and recip_for_div of them
   int part[MT];
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     sc[m] = 1.f;
+    rc[m] = 0.f;
     part[m] = 0;
   }
   // token and word index of flat word q
@@ -242,7 +243,10 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
     }
     if constexpr (!OUT_ACC) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m) sc[m] = m < M ? ld_cg_f32(scale_in + m) : 1.f;
+      for (int m = 0; m < MT; ++m) {
+        sc[m] = m < M ? ld_cg_f32(scale_in + m) : 1.f;
+        rc[m] = recip_for_div(sc[m]);
+      }
     }
   } else {
     XWord<XIN> cache[kCacheWords];
@@ -287,13 +291,12 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
       if (lane == 0) s_red[warp * MT + m] = v;
     }
     __syncthreads();
+    // each warp reduces the per-warp maxima itself: one load per lane, then shuffles
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float a = 0.f;
+    for (int m = 0; m < MT; ++m) sc[m] = token_scale(warp_max(lane < kWarps ? s_red[lane * MT + m] : 0.f));
+    // the reciprocals of the rescale, off the critical path of the output
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) a = fmaxf(a, s_red[w * MT + m]);
-      sc[m] = token_scale(a);
-    }
+    for (int m = 0; m < MT; ++m) rc[m] = recip_for_div(sc[m]);
     if (blockIdx.x == 0 && tid < M && scale_out) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
@@ -358,24 +361,36 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
     for (int i = 0; i < RB; ++i)
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[i][m][0] = acc[i][m][1] = acc[i][m][2] = acc[i][m][3] = 0;
-    for (int b = b0 + lane; b < b1; b += 32) {
+    // two blocks per iteration (b and b + 32) for independent loads; a block
+    // past the range reads block b again with its weights taken as zero
+    for (int b = b0 + lane; b < b1; b += 64) {
+      const bool two = b + 32 < b1;
+      const int b2 = two ? b + 32 : b;
       const uint32_t off = 4u * static_cast<uint32_t>(b - lane);
-      uint32_t wv[RB];
+      const uint32_t off2 = 4u * static_cast<uint32_t>(b2 - lane);
+      uint32_t wv[RB], wv2[RB];
 #pragma unroll
       for (int i = 0; i < RB; ++i) {
         const uint32_t w = lds_u32(ra[i] + off);
+        const uint32_t w2 = lds_u32(ra[i] + off2);
         wv[i] = rv[i] ? w : 0u;
+        wv2[i] = rv[i] && two ? w2 : 0u;
       }
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
         if (m < M) {
           const uint4 a = lds_v4(s_act32 + 16u * static_cast<uint32_t>(m * nblk + b));
+          const uint4 a2 = lds_v4(s_act32 + 16u * static_cast<uint32_t>(m * nblk + b2));
 #pragma unroll
           for (int i = 0; i < RB; ++i) {
             acc[i][m][0] = dp4a_us(wv[i] & 0x03030303u, static_cast<int>(a.x), acc[i][m][0]);
             acc[i][m][1] = dp4a_us(wv[i] & 0x0c0c0c0cu, static_cast<int>(a.y), acc[i][m][1]);
             acc[i][m][2] = dp4a_us(wv[i] & 0x30303030u, static_cast<int>(a.z), acc[i][m][2]);
             acc[i][m][3] = dp4a_us(wv[i] & 0xc0c0c0c0u, static_cast<int>(a.w), acc[i][m][3]);
+            acc[i][m][0] = dp4a_us(wv2[i] & 0x03030303u, static_cast<int>(a2.x), acc[i][m][0]);
+            acc[i][m][1] = dp4a_us(wv2[i] & 0x0c0c0c0cu, static_cast<int>(a2.y), acc[i][m][1]);
+            acc[i][m][2] = dp4a_us(wv2[i] & 0x30303030u, static_cast<int>(a2.z), acc[i][m][2]);
+            acc[i][m][3] = dp4a_us(wv2[i] & 0xc0c0c0c0u, static_cast<int>(a2.w), acc[i][m][3]);
           }
         }
       }
@@ -397,17 +412,14 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
 #pragma unroll
   for (int m = 0; m < MT; ++m) {
     if (m < M) {
-      int rs = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) rs += s_sum[w * MT + m];
-      const float rc = OUT_ACC ? 0.f : recip_for_div(sc[m]);
+      const int rs = __reduce_add_sync(0xffffffffu, lane < kWarps ? s_sum[lane * MT + m] : 0);
       for (int r = tid; r < R; r += kThreads) {
         const int a = s_acc[r * MT + m] - rs;
         const size_t o = static_cast<size_t>(m) * N + n0 + r;
         if constexpr (OUT_ACC) {
           static_cast<int32_t*>(out)[o] = a;
         } else {
-          static_cast<float*>(out)[o] = div_rn_recip(__fmul_rn(static_cast<float>(a), gm), sc[m], rc);
+          static_cast<float*>(out)[o] = div_rn_recip(__fmul_rn(static_cast<float>(a), gm), sc[m], rc[m]);
         }
       }
     }
