@@ -28,3 +28,12 @@ from .quantizer_variants import (  # noqa: F401,E402
     scaled_mean,
     threshold_quantize,
 )
+from .grouped import (  # noqa: F401,E402
+    GROUP,
+    bitlinear_forward_grouped,
+    group_accumulators,
+    group_codes,
+    group_gammas,
+    grouped_rescale,
+    grouped_y_bound,
+)
