@@ -60,6 +60,9 @@ def _load() -> ctypes.CDLL:
         "bitlinear_version": (ctypes.c_int, []),
         "bitlinear_device_error": (st, [ctypes.POINTER(ctypes.c_int)]),
         "bitlinear_tc_schedule": (st, [i64, i64, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int]),
+        "bitlinear_pack_weights_grouped": (st, [vp, i64, i64, vp, vp, vp]),
+        "bitlinear_forward_grouped_workspace_bytes": (sz, [i64, i64, i64]),
+        "bitlinear_forward_grouped": (st, [vp, ctypes.c_int, i64, vp, vp, i64, i64, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -281,6 +284,61 @@ def forward(x: torch.Tensor, packed: PackedWeight, y: Optional[torch.Tensor] = N
     return (y, xq, scale) if return_quant else y
 
 
+class PackedGrouped(NamedTuple):
+    """Per-group (64) packed ternary weights: wp uint8 [N][K/4] and gammas fp32 [N][K/64]."""
+
+    wp: torch.Tensor
+    gammas: torch.Tensor
+    n: int
+    k: int
+
+
+def pack_weights_grouped(w: torch.Tensor, out: Optional[PackedGrouped] = None) -> PackedGrouped:
+    """Per-group absmean quantisation (groups of 64 consecutive k of a row) and 2-bit packing."""
+    _cuda(w, "W", torch.float32)
+    if w.dim() != 2:
+        raise ValueError("W must be 2-D [N][K]")
+    n, k = w.shape
+    if out is None:
+        out = PackedGrouped(torch.empty((n, k // 4), dtype=torch.uint8, device=w.device),
+                            torch.empty((n, k // 64), dtype=torch.float32, device=w.device), n, k)
+    else:
+        _out(out.wp, "out.wp", torch.uint8, (n, k // 4), w.device)
+        _out(out.gammas, "out.gammas", torch.float32, (n, k // 64), w.device)
+    _check("bitlinear_pack_weights_grouped",
+           lib.bitlinear_pack_weights_grouped(w.data_ptr(), n, k, out.wp.data_ptr(), out.gammas.data_ptr(),
+                                              _stream(w.device)))
+    return out
+
+
+def forward_grouped(x: torch.Tensor, packed: PackedGrouped, y: Optional[torch.Tensor] = None,
+                    return_quant: bool = False, workspace: Optional[torch.Tensor] = None):
+    """y[m][n] = sum_g gammas[n][g] * acc[m][n][g] / s_m over per-group scales; fp32 [M][N]."""
+    _cuda(x, "x")
+    if x.dim() != 2 or x.shape[1] != packed.k:
+        raise ValueError(f"x must be [M][{packed.k}]")
+    m, k = x.shape
+    n = packed.n
+    _same_device(packed.wp, "packed.wp", x.device)
+    _same_device(packed.gammas, "packed.gammas", x.device)
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    else:
+        _out(y, "y", torch.float32, (m, n), x.device)
+    xq = scale = None
+    if return_quant:
+        xq = torch.empty((m, k), dtype=torch.int8, device=x.device)
+        scale = torch.empty(m, dtype=torch.float32, device=x.device)
+    hold, ws, wsn = _workspace(int(lib.bitlinear_forward_grouped_workspace_bytes(m, n, k)), x.device, workspace)
+    _check("bitlinear_forward_grouped",
+           lib.bitlinear_forward_grouped(x.data_ptr(), _dtype_code(x), m, packed.wp.data_ptr(),
+                                         packed.gammas.data_ptr(), n, k, y.data_ptr(),
+                                         xq.data_ptr() if xq is not None else None,
+                                         scale.data_ptr() if scale is not None else None, ws, wsn,
+                                         _stream(x.device)))
+    return (y, xq, scale) if return_quant else y
+
+
 def gemm_i32(xq: torch.Tensor, wp: torch.Tensor, acc: Optional[torch.Tensor] = None) -> torch.Tensor:
     """acc[m][n] = sum_k code[n][k] * xq[m][k] as exact int32."""
     _cuda(xq, "xq", torch.int8)
@@ -340,5 +398,5 @@ def tc_schedule(M: int, N: int, K: int, sms: int):
 
 
 __all__ = ["device_error", "PackedWeight", "BitLinearError", "pack_weights", "absmean", "quantize_pack", "quant_act", "forward",
-           "gemm", "gemm_i32",
+           "gemm", "gemm_i32", "PackedGrouped", "pack_weights_grouped", "forward_grouped",
            "pack_workspace_bytes", "forward_workspace_bytes", "tc_schedule", "TcPlan", "lib", "LIB_PATH"]

@@ -456,6 +456,49 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
   return launch_gemv(Wp, xq, sc, gamma, y, M, N, K, bl::GemvOut::kY, s);
 }
 
+bl_status bitlinear_pack_weights_grouped(const float* W, int64_t N, int64_t K, uint8_t* Wp, float* gammas,
+                                         bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_dims(1, N, K, false)) return st;
+  if (K % 64) return fail(BL_ERR_INVALID_ARG, "K=%lld is not a multiple of 64 (the group size)", (long long)K);
+  if (!W || !Wp || !gammas) return fail(BL_ERR_INVALID_ARG, "null pointer (W, Wp or gammas)");
+  if (!aligned(W, 16) || !aligned(Wp, 16) || !aligned(gammas, 4))
+    return fail(BL_ERR_INVALID_ARG, "W and Wp must be 16-byte aligned, gammas 4-byte aligned");
+  const cudaError_t e =
+      bl::launch_pack_grouped(W, N, K, Wp, gammas, sm_count(), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_pack_grouped: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
+size_t bitlinear_forward_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  if (M <= 0 || K <= 0) return 0;
+  return bl::forward_grouped_workspace(M, K);
+}
+
+bl_status bitlinear_forward_grouped(const void* x, bl_dtype dt, int64_t M, const uint8_t* Wp, const float* gammas,
+                                    int64_t N, int64_t K, float* y, int8_t* xq_out, float* scale_out, void* workspace,
+                                    size_t ws_bytes, bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_dims(M, N, K, true)) return st;
+  if (K % 64) return fail(BL_ERR_INVALID_ARG, "K=%lld is not a multiple of 64 (the group size)", (long long)K);
+  if (dt != BL_F32 && dt != BL_BF16) return fail(BL_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (M > 4 * 65535) return fail(BL_ERR_UNSUPPORTED, "M=%lld exceeds %d for the grouped forward", (long long)M, 4 * 65535);
+  if (!x || !Wp || !gammas || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (x, Wp, gammas or y)");
+  if (!aligned(x, 16) || !aligned(Wp, 16) || !aligned(y, 4) || !aligned(gammas, 4))
+    return fail(BL_ERR_INVALID_ARG, "x and Wp must be 16-byte aligned, y and gammas 4-byte aligned");
+  if (xq_out && !aligned(xq_out, 16)) return fail(BL_ERR_INVALID_ARG, "xq_out must be 16-byte aligned");
+  if (scale_out && !aligned(scale_out, 4)) return fail(BL_ERR_INVALID_ARG, "scale_out must be 4-byte aligned");
+  const size_t need = bitlinear_forward_grouped_workspace_bytes(M, N, K);
+  if (!workspace || !aligned(workspace, 256) || ws_bytes < need)
+    return fail(BL_ERR_WORKSPACE, "grouped forward workspace needs %zu bytes, 256-byte aligned", need);
+  const cudaError_t e =
+      bl::launch_forward_grouped(x, dt == BL_BF16, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), Wp,
+                                 gammas, y, xq_out, scale_out, workspace, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "grouped forward: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
 size_t bitlinear_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M <= 0 || N <= 0 || K <= 0) return 0;
   if (use_tc(M, K)) return tc_workspace_bytes(M, N, K);

@@ -139,6 +139,14 @@ cudaError_t launch_gemv_dp4a(const uint8_t* wp, const void* x, int xin, const fl
                              int rows_per_cta, size_t smem, cudaStream_t s);
 cudaError_t take_dp4a_wait_error(int* flag);
 
+// ---- per-group (64) packing and forward (grouped.cu)
+cudaError_t launch_pack_grouped(const float* W, int64_t N, int64_t K, uint8_t* wp, float* gam, int sms,
+                                cudaStream_t s);
+// Workspace of the grouped forward: transposed codes, group code sums, scales.
+size_t forward_grouped_workspace(int64_t M, int64_t K);
+cudaError_t launch_forward_grouped(const void* x, bool bf16, int M, int N, int K, const uint8_t* wp, const float* gam,
+                                   float* y, int8_t* xq_out, float* scale_out, void* ws, cudaStream_t s);
+
 // ---- prefill contraction on tcgen05 (prefill.cu)
 constexpr int kTcMinM = 17;   // smallest M routed to the tensor-core kernel (below it the
                               // mma.sync decode kernel is faster on B300)

@@ -268,6 +268,58 @@ BL_API bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp,
                              bl_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Per-group weight quantisation, groups of 64.
+ * Passage: "BitNet 1-bit LLM 的混合精度微调技术：渐进量化策略", body: per-group
+ * quantisation with a group size of 64. The page names the group size only;
+ * here a group is 64 consecutive k of one row, and each group takes the
+ * absmean rule of bitlinear_pack_weights on its own:
+ *   gamma[n][g] = exact mean of |W[n][64g .. 64g + 63]|, rounded once to fp32;
+ *   code = clip(rint(fp32(W / fp32(gamma[n][k / 64] + 1e-5))), -1, 1).
+ *
+ * W       fp32 [N][K] row-major, 16-byte aligned, finite, read only; K % 64 == 0.
+ * Wp      uint8 [N][K/4], 16-byte aligned, written: the per-tensor packing
+ *         layout (code of k = 4j + i in bits 2i..2i+1 of byte j of the row,
+ *         field = code + 1).
+ * gammas  fp32 [N][K/64] row-major, 4-byte aligned, written.
+ * No workspace; W is read once. Errors: BL_ERR_INVALID_ARG for null or
+ * misaligned pointers, non-positive sizes or K % 64 != 0; BL_ERR_UNSUPPORTED
+ * for K > 65536 or N*K >= 2^32; BL_ERR_CUDA if the launch fails.
+ * ------------------------------------------------------------------------- */
+BL_API bl_status bitlinear_pack_weights_grouped(const float* W, int64_t N, int64_t K,
+                                                uint8_t* Wp, float* gammas, bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * The forward over per-group scales:
+ *   y[m][n] = sum_g gammas[n][g] * acc[m][n][g] / s_m,
+ *   acc[m][n][g] = sum over group g of code * x_q (exact integers),
+ * with x_q and s_m the per-token absmax codes and scales of bitlinear_quant_act.
+ * Passages: as for bitlinear_pack_weights_grouped and bitlinear_forward.
+ *
+ * x          [M][K] row-major, fp32 or bf16 per `dt`, 16-byte aligned.
+ * Wp, gammas from bitlinear_pack_weights_grouped (K % 64 == 0).
+ * y          fp32 [M][N] row-major, 4-byte aligned, written. Each product
+ *            gamma * acc is exact in fp64; the K/64 products of a row are
+ *            added in fp64, divided by s_m in fp64 and rounded to fp32, so
+ *            |y - RN(exact / s_m)| <= ulp(y) + (K/64) 2^-52 sum_g |gamma * acc| / s_m.
+ * xq_out     optional int8 [M][K] (16-byte aligned) and scale_out optional
+ *            fp32 [M]: the quantised activations and scales, bit for bit those
+ *            of bitlinear_quant_act.
+ * workspace  at least bitlinear_forward_grouped_workspace_bytes(M, N, K)
+ *            bytes, 256-byte aligned; scratch. Calls that share a workspace
+ *            must not overlap on the GPU.
+ * Errors: as for bitlinear_forward, plus BL_ERR_INVALID_ARG for K % 64 != 0
+ * and BL_ERR_UNSUPPORTED for M > 262140.
+ * ------------------------------------------------------------------------- */
+BL_API size_t bitlinear_forward_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+BL_API bl_status bitlinear_forward_grouped(const void* x, bl_dtype dt, int64_t M,
+                                           const uint8_t* Wp, const float* gammas,
+                                           int64_t N, int64_t K, float* y,
+                                           int8_t* xq_out, float* scale_out,
+                                           void* workspace, size_t ws_bytes,
+                                           bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Schedule of the tensor-core contraction (the path of bitlinear_forward,
  * bitlinear_gemm and bitlinear_gemm_i32 for M >= 17 and K % 64 == 0), as a
  * test hook: host arithmetic only, no CUDA call, so it runs on any machine.

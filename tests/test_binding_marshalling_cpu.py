@@ -150,3 +150,24 @@ def test_gemm_marshalling(fake):
         blt.gemm_i32(xq, torch.zeros(8, 3, dtype=torch.uint8))
     with pytest.raises(TypeError):
         blt.gemm_i32(xq, packed.wp, acc=torch.empty(3, 8))
+
+
+def test_grouped_marshalling(fake):
+    blt, lib, torch = fake
+    w = torch.zeros(8, 128)
+    p = blt.pack_weights_grouped(w)
+    assert p.wp.shape == (8, 32) and p.gammas.shape == (8, 2) and p.gammas.dtype == torch.float32
+    a = last(lib, "bitlinear_pack_weights_grouped")
+    assert a == (w.data_ptr(), 8, 128, p.wp.data_ptr(), p.gammas.data_ptr(), 77)
+    out = blt.PackedGrouped(torch.empty(8, 32, dtype=torch.uint8), torch.empty(8, 2), 8, 128)
+    assert blt.pack_weights_grouped(w, out=out) is out
+    with pytest.raises(ValueError):
+        blt.pack_weights_grouped(w, out=blt.PackedGrouped(out.wp, torch.empty(8, 3), 8, 128))
+    x = torch.zeros(3, 128, dtype=torch.bfloat16)
+    y, xq, s = blt.forward_grouped(x, p, return_quant=True)
+    assert y.shape == (3, 8) and xq.shape == (3, 128) and s.shape == (3,)
+    a = last(lib, "bitlinear_forward_grouped")
+    assert a[:8] == (x.data_ptr(), blt.BL_BF16, 3, p.wp.data_ptr(), p.gammas.data_ptr(), 8, 128, y.data_ptr())
+    assert a[8] == xq.data_ptr() and a[9] == s.data_ptr() and a[10] % 256 == 0 and a[11] == 1024 and a[12] == 77
+    with pytest.raises(ValueError):
+        blt.forward_grouped(torch.zeros(3, 64), p)
