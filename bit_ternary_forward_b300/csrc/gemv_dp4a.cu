@@ -67,9 +67,10 @@ constexpr int kCopyThread = kThreads - 32;  // issues the weight copies (lane 0 
 // Set (never cleared by a kernel) when a bounded mbarrier wait gave up.
 __device__ int g_dp4a_wait_error;
 
-// Rows a warp works on at once: 4 accumulators per (row, token) stay in registers.
+// Rows a warp works on at once (4 accumulators per (row, token) in registers;
+// two rows keep the units small, so the warps' shares balance).
 template <int MT>
-constexpr int rows_per_batch() { return MT == 1 ? 4 : (MT == 2 ? 2 : 1); }
+constexpr int rows_per_batch() { return MT == 4 ? 1 : 2; }
 
 // Loads through L2 (not L1), issued after the dependency wait: the data may
 // have been written by the grid this one waited for.
@@ -501,7 +502,7 @@ size_t dp4a_act_bytes(int K, int mt) {
 }
 
 size_t dp4a_smem(int rows, int K, int mt) {
-  const int rb = mt == 1 ? 4 : (mt == 2 ? 2 : 1);   // rows_per_batch
+  const int rb = mt == 4 ? 1 : 2;   // rows_per_batch
   const size_t rowbytes = static_cast<size_t>(K) / 4;
   const size_t bpg = rb * rowbytes >= kGroupBytes ? 1 : kGroupBytes / (rb * rowbytes);
   const size_t rpg = bpg * rb;
