@@ -75,14 +75,16 @@ def row_bytes(p):
     forward: packed W, x and y once, gamma and the per-token scales.
     pack_weights: the compulsory traffic, W read once, Wp and gamma written."""
     nk, mk, mn = p.n * p.k, p.m * p.k, p.m * p.n
+    fwd = nk // 4 + x_bytes(p) * mk + 4 * mn + 4 + 4 * p.m
     return {
-        "forward": nk // 4 + x_bytes(p) * mk + 4 * mn + 4 + 4 * p.m,
+        "forward": fwd,
+        "forward_lut": fwd,
         "pack_weights": 4 * nk + nk // 4 + 4,
     }
 
 
 def row_ops(p):
-    return {"forward": 2 * p.m * p.n * p.k}
+    return {"forward": 2 * p.m * p.n * p.k, "forward_lut": 2 * p.m * p.n * p.k}
 
 
 def row_kernels(p):
@@ -100,7 +102,7 @@ def row_kernels(p):
         fwd = ["bl_act_quant", "bl_decode_mma"]
     else:
         fwd = ["bl_act_quant", "bl_gemv_w2a8"]
-    return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"], "forward": fwd}
+    return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"], "forward": fwd, "forward_lut": ["bl_gemv_lut"]}
 
 
 def workload_units(projs, unit, rows=("forward",)):
@@ -411,6 +413,7 @@ class ForwardSet:
     def __init__(self, blt, projs, device, slots):
         from workloads.synth import gaussian_activations_on, student_t_weights_on
         self.blt, self.lib, self.projs, self.device = blt, blt.lib, projs, device
+        self.lut = False          # calls go to bitlinear_forward_lut (the table-lookup GEMV) when set
         self.slots = []
         for r in range(slots):
             slot = []
@@ -453,7 +456,11 @@ class ForwardSet:
                 _check(lib, lib.bitlinear_forward(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(),
                                                   d["gamma"].data_ptr(), p.n, p.k, d["y"].data_ptr(), None, None,
                                                   d["ws"], d["nws"], st))
-            out.append((p, call))
+
+            def call_lut(st, d=d, p=p):
+                _check(lib, lib.bitlinear_forward_lut(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(),
+                                                      d["gamma"].data_ptr(), p.n, p.k, d["y"].data_ptr(), st))
+            out.append((p, call_lut if self.lut else call))
         return out
 
     def weight_bytes_per_slot(self):
@@ -714,6 +721,39 @@ def measure_forward(blt, wl, device, stream, args, world, hbm, bf16, bf16_sus, p
             "slot_bytes": sum(4 * p.m * p.n + x_bytes(p) * p.m * p.k + p.n * p.k // 4 for p in wl.projections)}
 
 
+LUT_MAX_K = 16384
+
+
+def lut_applies(wl):
+    return all(p.m == 1 and p.k % 64 == 0 and p.k <= LUT_MAX_K for p in wl.projections)
+
+
+def measure_lut(fs, wl, device, stream, args, world, hbm, dp4a_value):
+    """The same decode step through the table-lookup GEMV (bitlinear_forward_lut),
+    timed the same way on the same rotating slots, for the comparison with the
+    dp4a GEMV of the main line."""
+    fs.lut = True
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                for _, call in fs.calls(i):
+                    call(stream.cuda_stream)
+        stream.synchronize()
+        G = graph_steps_for(args.steps, args.graph_steps)
+        graph, _ = capture(fs, G, stream)
+        marked, pool = capture(fs, G, stream, marked=True)
+        ms = time_graph(graph, args.steps // G, stream, world, device)
+        per_call = per_call_ms(fs, marked, pool, G, stream)
+    finally:
+        fs.lut = False
+    units_step = workload_units(wl.projections, "GB/s", rows=("forward_lut",))
+    value = world * units_step * args.steps / (ms * 1e-3) / 1e9
+    row = row_entry("forward by table lookup (alternative kernel, each call alone)", per_call, "forward_lut", hbm)
+    return {"kernel": "bl_gemv_lut", "value": value, "unit": "GB/s", "frac": value / hbm,
+            "ms_per_step": ms / args.steps, "alone_us": row["avg_us"], "vs_dp4a": value / dp4a_value,
+            "timing": "the main line's method on the same slots: graph of the step's calls, no event nodes"}, row
+
+
 def measure_pack(blt, wl, device, stream, args, world, hbm):
     """Per-call time of bitlinear_pack_weights on the workload's weights (two
     rotating fp32 copies, each larger than L2 for the 2B shapes)."""
@@ -791,10 +831,14 @@ def main(argv=None):
     rows = [dict(main_res["row"], row="forward (all calls of the step, each alone)")] + main_res["rows_by_projection"]
 
     e2e = run_e2e(blt, main_res["fs"], wl.projections, device, stream, args.e2e_steps, main_res["unit"])
+    companions = {}
+    if decode and not args.no_companions and lut_applies(wl):
+        companions["lut_gemv"], lut_row = measure_lut(main_res["fs"], wl, device, stream, args, world, hbm,
+                                                      main_res["value"])
+        rows.append(lut_row)
     del main_res["fs"]
     torch.cuda.empty_cache()
 
-    companions = {}
     if not args.no_companions and wl.layers == 1 and wl.name != "cpu_small":
         rows.append(measure_pack(blt, wl, device, stream, args, world, hbm))
         if decode and wl.name == "decode_2b":

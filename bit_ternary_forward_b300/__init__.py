@@ -60,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "bitlinear_version": (ctypes.c_int, []),
         "bitlinear_device_error": (st, [ctypes.POINTER(ctypes.c_int)]),
         "bitlinear_tc_schedule": (st, [i64, i64, i64, ctypes.c_int, vp, vp, vp, ctypes.c_int]),
+        "bitlinear_forward_lut": (st, [vp, ctypes.c_int, i64, vp, vp, i64, i64, vp, vp]),
         "bitlinear_pack_weights_grouped": (st, [vp, i64, i64, vp, vp, vp]),
         "bitlinear_forward_grouped_workspace_bytes": (sz, [i64, i64, i64]),
         "bitlinear_forward_grouped": (st, [vp, ctypes.c_int, i64, vp, vp, i64, i64, vp, vp, vp, vp, sz, vp]),
@@ -284,6 +285,25 @@ def forward(x: torch.Tensor, packed: PackedWeight, y: Optional[torch.Tensor] = N
     return (y, xq, scale) if return_quant else y
 
 
+def forward_lut(x: torch.Tensor, packed: PackedWeight, y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The one-token forward by table lookup (bitlinear_forward_lut); same y as forward, bit for bit."""
+    _cuda(x, "x")
+    if x.dim() != 2 or x.shape[1] != packed.k:
+        raise ValueError(f"x must be [1][{packed.k}]")
+    m, k = x.shape
+    n = packed.n
+    _same_device(packed.wp, "packed.wp", x.device)
+    _same_device(packed.gamma, "packed.gamma", x.device)
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    else:
+        _out(y, "y", torch.float32, (m, n), x.device)
+    _check("bitlinear_forward_lut",
+           lib.bitlinear_forward_lut(x.data_ptr(), _dtype_code(x), m, packed.wp.data_ptr(), packed.gamma.data_ptr(),
+                                     n, k, y.data_ptr(), _stream(x.device)))
+    return y
+
+
 class PackedGrouped(NamedTuple):
     """Per-group (64) packed ternary weights: wp uint8 [N][K/4] and gammas fp32 [N][K/64]."""
 
@@ -398,5 +418,5 @@ def tc_schedule(M: int, N: int, K: int, sms: int):
 
 
 __all__ = ["device_error", "PackedWeight", "BitLinearError", "pack_weights", "absmean", "quantize_pack", "quant_act", "forward",
-           "gemm", "gemm_i32", "PackedGrouped", "pack_weights_grouped", "forward_grouped",
+           "gemm", "gemm_i32", "forward_lut", "PackedGrouped", "pack_weights_grouped", "forward_grouped",
            "pack_workspace_bytes", "forward_workspace_bytes", "tc_schedule", "TcPlan", "lib", "LIB_PATH"]

@@ -456,6 +456,23 @@ bl_status bitlinear_forward(const void* x, bl_dtype dt, int64_t M, const uint8_t
   return launch_gemv(Wp, xq, sc, gamma, y, M, N, K, bl::GemvOut::kY, s);
 }
 
+bl_status bitlinear_forward_lut(const void* x, bl_dtype dt, int64_t M, const uint8_t* Wp, const float* gamma,
+                                int64_t N, int64_t K, float* y, bl_stream_t stream) {
+  g_last_error.clear();
+  if (bl_status st = check_dims(M, N, K, true)) return st;
+  if (M != 1) return fail(BL_ERR_UNSUPPORTED, "the lookup-table GEMV takes one token (M=%lld)", (long long)M);
+  if (K % 64) return fail(BL_ERR_INVALID_ARG, "K=%lld is not a multiple of 64", (long long)K);
+  if (K > bl::kLutMaxK) return fail(BL_ERR_UNSUPPORTED, "K=%lld exceeds %d for the lookup-table GEMV", (long long)K, bl::kLutMaxK);
+  if (dt != BL_F32 && dt != BL_BF16) return fail(BL_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
+  if (!x || !Wp || !gamma || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (x, Wp, gamma or y)");
+  if (!aligned(x, 16) || !aligned(Wp, 16) || !aligned(y, 4) || !aligned(gamma, 4))
+    return fail(BL_ERR_INVALID_ARG, "x and Wp must be 16-byte aligned, y and gamma 4-byte aligned");
+  const cudaError_t e = bl::launch_gemv_lut(Wp, x, dt == BL_BF16, gamma, y, static_cast<int>(N), static_cast<int>(K),
+                                            sm_count(), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(BL_ERR_CUDA, "bl_gemv_lut: %s", cudaGetErrorString(e));
+  return BL_OK;
+}
+
 bl_status bitlinear_pack_weights_grouped(const float* W, int64_t N, int64_t K, uint8_t* Wp, float* gammas,
                                          bl_stream_t stream) {
   g_last_error.clear();

@@ -139,6 +139,12 @@ cudaError_t launch_gemv_dp4a(const uint8_t* wp, const void* x, int xin, const fl
                              int rows_per_cta, size_t smem, cudaStream_t s);
 cudaError_t take_dp4a_wait_error(int* flag);
 
+// ---- lookup-table decode GEMV, one token (gemv_lut.cu)
+constexpr int kLutMaxK = 16384;
+size_t gemv_lut_smem(int K);
+cudaError_t launch_gemv_lut(const uint8_t* wp, const void* x, bool bf16, const float* gamma, float* y, int N, int K,
+                            int sms, cudaStream_t s);
+
 // ---- per-group (64) packing and forward (grouped.cu)
 cudaError_t launch_pack_grouped(const float* W, int64_t N, int64_t K, uint8_t* wp, float* gam, int sms,
                                 cudaStream_t s);

@@ -268,6 +268,26 @@ BL_API bl_status bitlinear_gemm_i32(const int8_t* xq, const uint8_t* Wp,
                              bl_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * The forward for one token by table lookup: the table idea of bitnet.cpp's
+ * TL1 kernel ("部署 BitNet 1-bit LLM：三元权重边缘推理优化", kernel types; TL1
+ * uses a lookup table), as an alternative to the dp4a GEMV of
+ * bitlinear_forward, with the same result bit for bit. For every pair of
+ * consecutive inputs the kernel tabulates the nine partial sums
+ * (f0 - 1) x_q[2p] + (f1 - 1) x_q[2p + 1] once per call; each 4-bit nibble
+ * of a packed row then selects one entry.
+ *
+ * x      [1][K] fp32 or bf16 per `dt`, 16-byte aligned; M must be 1.
+ * Wp, gamma from bitlinear_pack_weights; K % 64 == 0, K <= 16384.
+ * y      fp32 [1][N], 4-byte aligned, written: fp32(fp32(acc * gamma) / s).
+ * No workspace. Errors: BL_ERR_UNSUPPORTED for M != 1 or K > 16384;
+ * otherwise as for bitlinear_forward.
+ * ------------------------------------------------------------------------- */
+BL_API bl_status bitlinear_forward_lut(const void* x, bl_dtype dt, int64_t M,
+                                       const uint8_t* Wp, const float* gamma,
+                                       int64_t N, int64_t K, float* y,
+                                       bl_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Per-group weight quantisation, groups of 64.
  * Passage: "BitNet 1-bit LLM 的混合精度微调技术：渐进量化策略", body: per-group
  * quantisation with a group size of 64. The page names the group size only;

@@ -48,7 +48,11 @@ def test_workload_units_sums_the_forward_bytes():
     projs = [proj(1, 2560, 6912), proj(1, 6912, 2560)]
     assert bench.workload_units(projs, "GB/s") == sum(bench.row_bytes(p)["forward"] for p in projs)
     assert bench.workload_units(projs, "GB/s", rows=("forward", "pack_weights")) == \
-        sum(sum(bench.row_bytes(p).values()) for p in projs)
+        sum(bench.row_bytes(p)["forward"] + bench.row_bytes(p)["pack_weights"] for p in projs)
+    # the table-lookup alternative moves the same algorithmic bytes as the dp4a forward
+    assert all(bench.row_bytes(p)["forward_lut"] == bench.row_bytes(p)["forward"] for p in projs)
+    assert bench.lut_applies(bench.WORKLOADS["decode_2b"]) and bench.lut_applies(bench.WORKLOADS["stack_7b_decode"])
+    assert not bench.lut_applies(bench.WORKLOADS["prefill_2b"])
 
 
 def test_rotation_covers_twice_the_l2(monkeypatch):

@@ -171,3 +171,15 @@ def test_grouped_marshalling(fake):
     assert a[8] == xq.data_ptr() and a[9] == s.data_ptr() and a[10] % 256 == 0 and a[11] == 1024 and a[12] == 77
     with pytest.raises(ValueError):
         blt.forward_grouped(torch.zeros(3, 64), p)
+
+
+def test_forward_lut_marshalling(fake):
+    blt, lib, torch = fake
+    p = blt.PackedWeight(torch.empty(8, 32, dtype=torch.uint8), torch.empty(1), 8, 128)
+    x = torch.zeros(1, 128)
+    y = blt.forward_lut(x, p)
+    assert y.shape == (1, 8)
+    a = last(lib, "bitlinear_forward_lut")
+    assert a == (x.data_ptr(), blt.BL_F32, 1, p.wp.data_ptr(), p.gamma.data_ptr(), 8, 128, y.data_ptr(), 77)
+    with pytest.raises(ValueError):
+        blt.forward_lut(torch.zeros(1, 64), p)
