@@ -79,12 +79,14 @@ def row_bytes(p):
     return {
         "forward": fwd,
         "forward_lut": fwd,
+        "forward_grouped": fwd + nk // 16 - 4,             # per-group scales in place of one gamma
         "pack_weights": 4 * nk + nk // 4 + 4,
+        "pack_grouped": 4 * nk + nk // 4 + nk // 16,
     }
 
 
 def row_ops(p):
-    return {"forward": 2 * p.m * p.n * p.k, "forward_lut": 2 * p.m * p.n * p.k}
+    return {"forward": 2 * p.m * p.n * p.k, "forward_lut": 2 * p.m * p.n * p.k, "forward_grouped": 2 * p.m * p.n * p.k}
 
 
 def row_kernels(p):
@@ -102,7 +104,8 @@ def row_kernels(p):
         fwd = ["bl_act_quant", "bl_decode_mma"]
     else:
         fwd = ["bl_act_quant", "bl_gemv_w2a8"]
-    return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"], "forward": fwd, "forward_lut": ["bl_gemv_lut"]}
+    return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"], "forward": fwd, "forward_lut": ["bl_gemv_lut"],
+            "forward_grouped": ["bl_act_quant_grouped", "bl_gemv_grouped"], "pack_grouped": ["bl_pack_grouped"]}
 
 
 def workload_units(projs, unit, rows=("forward",)):
@@ -414,6 +417,7 @@ class ForwardSet:
         from workloads.synth import gaussian_activations_on, student_t_weights_on
         self.blt, self.lib, self.projs, self.device = blt, blt.lib, projs, device
         self.lut = False          # calls go to bitlinear_forward_lut (the table-lookup GEMV) when set
+        self.grouped = False      # calls go to bitlinear_forward_grouped (per-group scales) when set
         self.slots = []
         for r in range(slots):
             slot = []
@@ -460,8 +464,31 @@ class ForwardSet:
             def call_lut(st, d=d, p=p):
                 _check(lib, lib.bitlinear_forward_lut(d["x"].data_ptr(), d["xdt"], p.m, d["wp"].data_ptr(),
                                                       d["gamma"].data_ptr(), p.n, p.k, d["y"].data_ptr(), st))
-            out.append((p, call_lut if self.lut else call))
+
+            def call_grouped(st, d=d, p=p):
+                _check(lib, lib.bitlinear_forward_grouped(d["x"].data_ptr(), d["xdt"], p.m, d["wpg"].data_ptr(),
+                                                          d["gammas"].data_ptr(), p.n, p.k, d["y"].data_ptr(), None,
+                                                          None, d["gws"], d["ngws"], st))
+            out.append((p, call_grouped if self.grouped else (call_lut if self.lut else call)))
         return out
+
+    def add_grouped(self):
+        """Per-group packed weights of every projection (slot 0 packed from the
+        seeded W, the other slots copies) and the grouped forward's workspaces."""
+        blt = self.blt
+        for j, p in enumerate(self.projs):
+            w, _ = make_projection_inputs(p)
+            g = blt.pack_weights_grouped(w.to(self.device))
+            torch.cuda.synchronize(self.device)
+            del w
+            for r, slot in enumerate(self.slots):
+                d = slot[j]
+                d["wpg"] = g.wp if r == 0 else g.wp.clone()
+                d["gammas"] = g.gammas if r == 0 else g.gammas.clone()
+                n = int(blt.lib.bitlinear_forward_grouped_workspace_bytes(p.m, p.n, p.k))
+                d["gws_t"] = torch.empty(n + 256, dtype=torch.uint8, device=self.device)
+                d["gws"] = (d["gws_t"].data_ptr() + 255) // 256 * 256
+                d["ngws"] = n
 
     def weight_bytes_per_slot(self):
         return sum(p.n * p.k // 4 for p in self.projs)
@@ -754,6 +781,79 @@ def measure_lut(fs, wl, device, stream, args, world, hbm, dp4a_value):
             "timing": "the main line's method on the same slots: graph of the step's calls, no event nodes"}, row
 
 
+def grouped_applies(wl):
+    return all(p.k % 64 == 0 for p in wl.projections)
+
+
+def measure_grouped(fs, wl, device, stream, args, world, hbm, dp4a_value):
+    """The same step through the per-group forward (bitlinear_forward_grouped)
+    on per-group packed copies of the workload's weights, timed the same way."""
+    fs.add_grouped()
+    fs.grouped = True
+    try:
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                for _, call in fs.calls(i):
+                    call(stream.cuda_stream)
+        stream.synchronize()
+        G = graph_steps_for(args.steps, args.graph_steps)
+        graph, _ = capture(fs, G, stream)
+        marked, pool = capture(fs, G, stream, marked=True)
+        ms = time_graph(graph, args.steps // G, stream, world, device)
+        per_call = per_call_ms(fs, marked, pool, G, stream)
+    finally:
+        fs.grouped = False
+    unit = unit_of(wl)
+    rows = ("forward_grouped",)
+    units_step = (workload_units(wl.projections, "GB/s", rows=rows) if unit == "GB/s"
+                  else sum(row_ops(p)["forward_grouped"] for p in wl.projections))
+    value = world * units_step * args.steps / (ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    row = row_entry("forward with per-group (64) scales (each call alone)", per_call, "forward_grouped", hbm)
+    return {"kernels": ["bl_act_quant_grouped", "bl_gemv_grouped"], "value": value, "unit": unit,
+            "frac": value / hbm if unit == "GB/s" else None, "ms_per_step": ms / args.steps,
+            "alone_us": row["avg_us"], "vs_per_tensor": value / dp4a_value,
+            "timing": "the main line's method on the same slots: graph of the step's calls, no event nodes"}, row
+
+
+def measure_pack_grouped(blt, wl, device, stream, hbm):
+    """Per-call time of bitlinear_pack_weights_grouped on the workload's fp32
+    weights (two rotating copies)."""
+    ps = PackSet(blt, wl.projections, device, 2)
+    for slot in ps.slots:
+        for d in slot:
+            d["gam_g"] = torch.empty((d["p"].n, d["p"].k // 64), dtype=torch.float32, device=device)
+    lib = blt.lib
+
+    class _Grouped:
+        projs = ps.projs
+
+        @staticmethod
+        def calls(i):
+            out = []
+            for d in ps.slots[i % len(ps.slots)]:
+                p = d["p"]
+
+                def call(st, d=d, p=p):
+                    _check(lib, lib.bitlinear_pack_weights_grouped(d["w"].data_ptr(), p.n, p.k, d["wp"].data_ptr(),
+                                                                   d["gam_g"].data_ptr(), st))
+                out.append((p, call))
+            return out
+    gs = _Grouped()
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            for _, call in gs.calls(i):
+                call(stream.cuda_stream)
+    stream.synchronize()
+    G = 8
+    marked, pool = capture(gs, G, stream, marked=True)
+    per_call = per_call_ms(gs, marked, pool, G, stream)
+    e = row_entry("pack_weights_grouped (one-time, outside the step)", per_call, "pack_grouped", hbm)
+    e["bytes_note"] = "compulsory 4*N*K + N*K/4 + N*K/16 (W read once, Wp and the scales written)"
+    del ps
+    torch.cuda.empty_cache()
+    return e
+
+
 def measure_pack(blt, wl, device, stream, args, world, hbm):
     """Per-call time of bitlinear_pack_weights on the workload's weights (two
     rotating fp32 copies, each larger than L2 for the 2B shapes)."""
@@ -836,11 +936,17 @@ def main(argv=None):
         companions["lut_gemv"], lut_row = measure_lut(main_res["fs"], wl, device, stream, args, world, hbm,
                                                       main_res["value"])
         rows.append(lut_row)
+    if not args.no_companions and wl.layers == 1 and wl.name != "cpu_small" and grouped_applies(wl):
+        companions["per_group"], g_row = measure_grouped(main_res["fs"], wl, device, stream, args, world, hbm,
+                                                         main_res["value"])
+        rows.append(g_row)
     del main_res["fs"]
     torch.cuda.empty_cache()
 
     if not args.no_companions and wl.layers == 1 and wl.name != "cpu_small":
         rows.append(measure_pack(blt, wl, device, stream, args, world, hbm))
+        if grouped_applies(wl):
+            rows.append(measure_pack_grouped(blt, wl, device, stream, hbm))
         if decode and wl.name == "decode_2b":
             pwl = WORKLOADS[PREFILL_COMPANION]
             pslots = prefill_slots(pwl, device)

@@ -155,3 +155,48 @@ def test_peaks_come_from_the_measured_file():
     d = json.load(open(path))
     assert source == "measured" and hbm == float(d["hbm_gbs"]) and bf16 == float(d["bf16_tflops"])
     assert sustained <= bf16
+
+
+def test_step_sets_build_every_call_kind_on_cpu(monkeypatch):
+    """ForwardSet and PackSet with a stand-in library on CPU tensors: every
+    call kind (dp4a forward, table lookup, per-group) is built and callable."""
+    import torch
+    calls = []
+
+    class FakeLib:
+        def __getattr__(self, name):
+            def f(*a):
+                calls.append(name)
+                return 1024 if name.endswith("_workspace_bytes") else 0
+            return f
+
+    class Grouped:
+        def __init__(self, n, k):
+            self.wp = torch.zeros(n, k // 4, dtype=torch.uint8)
+            self.gammas = torch.zeros(n, k // 64)
+
+    class FakeBlt:
+        lib = FakeLib()
+        BL_BF16, BL_F32 = 1, 0
+        forward_workspace_bytes = staticmethod(lambda m, n, k: 1024)
+        pack_workspace_bytes = staticmethod(lambda n, k: 1024)
+        PackedWeight = staticmethod(lambda *a: a)
+        pack_weights = staticmethod(lambda w, out=None: out)
+        pack_weights_grouped = staticmethod(lambda w: Grouped(*w.shape))
+
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda *a, **k: None)
+    wl = bench.WORKLOADS["cpu_small"]
+    fs = bench.ForwardSet(FakeBlt, wl.projections, torch.device("cpu"), 2)
+    for _, c in fs.calls(0):
+        c(0)
+    fs.lut = True
+    for _, c in fs.calls(1):
+        c(0)
+    fs.lut = False
+    fs.add_grouped()
+    fs.grouped = True
+    for _, c in fs.calls(1):
+        c(0)
+    assert [n for n in calls if n in ("bitlinear_forward", "bitlinear_forward_lut", "bitlinear_forward_grouped")] == \
+        ["bitlinear_forward", "bitlinear_forward_lut", "bitlinear_forward_grouped"]
+    assert len(bench.PackSet(FakeBlt, wl.projections, torch.device("cpu"), 2).calls(0)) == len(wl.projections)
