@@ -500,7 +500,7 @@ bl_status bitlinear_forward_grouped(const void* x, bl_dtype dt, int64_t M, const
   if (bl_status st = check_dims(M, N, K, true)) return st;
   if (K % 64) return fail(BL_ERR_INVALID_ARG, "K=%lld is not a multiple of 64 (the group size)", (long long)K);
   if (dt != BL_F32 && dt != BL_BF16) return fail(BL_ERR_INVALID_ARG, "unknown dtype %d", (int)dt);
-  if (M > 4 * 65535) return fail(BL_ERR_UNSUPPORTED, "M=%lld exceeds %d for the grouped forward", (long long)M, 4 * 65535);
+  if (M > 65535) return fail(BL_ERR_UNSUPPORTED, "M=%lld exceeds 65535 for the grouped forward", (long long)M);
   if (!x || !Wp || !gammas || !y) return fail(BL_ERR_INVALID_ARG, "null pointer (x, Wp, gammas or y)");
   if (!aligned(x, 16) || !aligned(Wp, 16) || !aligned(y, 4) || !aligned(gammas, 4))
     return fail(BL_ERR_INVALID_ARG, "x and Wp must be 16-byte aligned, y and gammas 4-byte aligned");

@@ -25,15 +25,16 @@
 // 2^-149. Either sum times the unit over 64 is rounded once to fp32 (ties to
 // even), with every dropped bit kept as a sticky bit.
 //
-// The forward: the activation pass and the packed-word contraction are those
-// of the decode GEMV (per-token absmax codes; four field planes per packed
-// word in one dp4a each), but each 16-code block's partial sum is completed
-// on its own (minus the block's activation sum, as fields are codes + 1),
-// four lanes (one group) are added by shuffles, and the group sum times its
-// scale is accumulated in fp64: each product is exact (24-bit scale times a
-// sum below 2^14), and the fp64 sum over the K/64 groups of a row carries a
-// relative error below (K/64) 2^-53 of sum_g |gamma * acc|. y is the fp64
-// sum divided by s_m in fp64 and rounded to fp32.
+// The forward: per-token absmax codes (as in the per-tensor forward, stored
+// in the transposed block layout with the code sum of every group), then a
+// contraction over tiles of 32 weight rows x up to 8 tokens with the tile's
+// codes staged in shared memory: per group, the four packed words meet the
+// four activation blocks plane by plane in dp4a (fields are codes + 1, so the
+// group's code sum is taken off), and the group sum times its scale is
+// accumulated in fp64: each product is exact (24-bit scale times a sum below
+// 2^14), and the fp64 sum over the K/64 groups of a row carries a relative
+// error below (K/64) 2^-53 of sum_g |gamma * acc|. y is the fp64 sum divided
+// by s_m in fp64 and rounded to fp32.
 
 #include "async.cuh"
 #include "common.cuh"
@@ -168,10 +169,17 @@ bl_pack_grouped(const float4* __restrict__ w4, uint64_t n_groups, uint8_t* __res
   const int lane = threadIdx.x & 31;
   const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (kGpThreads / 32);
   const uint64_t wid = static_cast<uint64_t>(blockIdx.x) * (kGpThreads / 32) + (threadIdx.x >> 5);
+  auto load = [&](uint64_t pair) {
+    const uint64_t g = pair + (lane >> 4);
+    return g < n_groups ? __ldcs(w4 + g * 16 + (lane & 15)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  // the next pair's weights are loaded before this pair's arithmetic
+  float4 next = load(2 * wid);
   for (uint64_t pair0 = 2 * wid; pair0 < n_groups; pair0 += 2 * warps) {
     const uint64_t g = pair0 + (lane >> 4);
     const bool live = g < n_groups;                     // the last pair may hold one group
-    const float4 v = live ? __ldcs(w4 + g * 16 + (lane & 15)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 v = next;
+    next = load(pair0 + 2 * warps);
     const float gamma = group_gamma(v, lane);
     if (!live) continue;
     const float h = __fmul_rn(__fadd_rn(gamma, kEpsGamma), 0.5f);   // d / 2, d = fp32(gamma + 1e-5) >= 1e-5
@@ -195,7 +203,8 @@ cudaError_t launch_pack_grouped(const float* W, int64_t N, int64_t K, uint8_t* w
 namespace {
 
 constexpr int kGaThreads = 256;             // activation pass: one CTA per token
-constexpr int kGfWarps = 8;                 // contraction: one warp per (row, token tile)
+constexpr int kGThreads = 256;              // contraction: 8 warps (k-slices) x 32 rows
+constexpr size_t kGMaxSmem = 200 * 1024;
 
 // Loads through L2 (not L1): the data may have been written by the grid this
 // one waited for.
@@ -303,60 +312,94 @@ bl_act_quant_grouped(const T* __restrict__ x, int K, uint4* __restrict__ xt, int
   }
 }
 
-// y[m][n] for the tokens m0 .. m0 + MT - 1 of blockIdx.y and the row n of
-// this warp: lanes take groups g = lane, lane + 32, ...; per group the four
-// packed words (blocks 4g .. 4g + 3) meet the four transposed activation
-// blocks plane by plane (dp4a), the group's code sum is taken off, and the
-// group sum times gamma[n][g] is added in fp64.
-template <int MT>
-__global__ void __launch_bounds__(kGfWarps * 32)
-bl_gemv_grouped(const uint8_t* __restrict__ wp, const float* __restrict__ gam, const uint4* __restrict__ xt,
+// y[m][n] for a tile of 32 weight rows x TM tokens. The tile's transposed
+// codes and group code sums are staged in shared memory once; warp w takes
+// the groups g = w, w + 8, ... and lane l the row n0 + l, so the 32 lanes of
+// a read of the activations read the same word (a broadcast). Per group the
+// four packed words of the row (one 16-byte load) meet the four activation
+// blocks plane by plane (dp4a), the group's code sum is taken off, and
+// gamma[n][g] * acc is added in fp64 (exact product). The eight warps'
+// partial sums of a (row, token) are added in a fixed order, then divided
+// by s_m in fp64 and rounded to fp32.
+constexpr int kGRows = 32;
+constexpr int kGSlices = kGThreads / 32;
+
+size_t gemm_grouped_smem(int K, int tm) {
+  return static_cast<size_t>(tm) * K + static_cast<size_t>(tm) * (K / 64) * 4 +
+         static_cast<size_t>(kGSlices) * kGRows * tm * 8 + 16;
+}
+
+template <int TM>
+__global__ void __launch_bounds__(kGThreads)
+bl_gemm_grouped(const uint8_t* __restrict__ wp, const float* __restrict__ gam, const uint4* __restrict__ xt,
                 const int* __restrict__ gsum, const float* __restrict__ scale, float* __restrict__ y, int M, int N,
                 int K) {
+  extern __shared__ __align__(16) uint8_t smem[];
   pdl_wait();
   pdl_launch_dependents();
   xt = launder(xt);
   gsum = launder(gsum);
   scale = launder(scale);
-  const int lane = threadIdx.x & 31;
-  const int n = blockIdx.x * kGfWarps + (threadIdx.x >> 5);
-  if (n >= N) return;
-  const int m0 = blockIdx.y * MT;
-  const int G = K >> 6;
-  const uint4* wrow = reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 2));
-  const float* grow = gam + static_cast<size_t>(n) * G;
-  double acc[MT];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int G = K >> 6, nblk = K >> 4;
+  const int m0 = blockIdx.y * TM;
+  const int tm = min(TM, M - m0);
+  uint4* s_x = reinterpret_cast<uint4*>(smem);                                   // [TM][K/16]
+  int* s_gs = reinterpret_cast<int*>(smem + static_cast<size_t>(TM) * K);        // [TM][G]
+  double* s_part = reinterpret_cast<double*>(
+      (reinterpret_cast<uintptr_t>(s_gs + TM * G) + 7) & ~uintptr_t(7));         // [slices][rows][TM]
+  for (int i = tid; i < tm * nblk; i += kGThreads) s_x[i] = ldg_cg_v4(xt + static_cast<size_t>(m0) * nblk + i);
+  for (int i = tid; i < tm * G; i += kGThreads) s_gs[i] = __ldcg(gsum + static_cast<size_t>(m0) * G + i);
+  __syncthreads();
+  const int n = blockIdx.x * kGRows + lane;
+  double acc[TM];
 #pragma unroll
-  for (int t = 0; t < MT; ++t) acc[t] = 0.0;
-  for (int g = lane; g < G; g += 32) {
-    const uint4 w = __ldg(wrow + g);
-    const double gm = static_cast<double>(__ldg(grow + g));
-    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+  for (int t = 0; t < TM; ++t) acc[t] = 0.0;
+  if (n < N) {
+    const uint4* wrow = reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 2));
+    const float* grow = gam + static_cast<size_t>(n) * G;
+    for (int g = warp; g < G; g += kGSlices) {
+      const uint4 w = __ldg(wrow + g);
+      const double gm = static_cast<double>(__ldg(grow + g));
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+      uint32_t pl[4][4];
 #pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      const int m = m0 + t;
-      if (m < M) {
-        const uint4* xb = xt + static_cast<size_t>(m) * (K >> 4) + 4 * g;
-        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+      for (int j = 0; j < 4; ++j) {
+        pl[j][0] = wv[j] & 0x03030303u;
+        pl[j][1] = wv[j] & 0x0c0c0c0cu;
+        pl[j][2] = wv[j] & 0x30303030u;
+        pl[j][3] = wv[j] & 0xc0c0c0c0u;
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 a = ldg_cg_v4(xb + j);
-          a0 = dp4a_us(wv[j] & 0x03030303u, static_cast<int>(a.x), a0);
-          a1 = dp4a_us(wv[j] & 0x0c0c0c0cu, static_cast<int>(a.y), a1);
-          a2 = dp4a_us(wv[j] & 0x30303030u, static_cast<int>(a.z), a2);
-          a3 = dp4a_us(wv[j] & 0xc0c0c0c0u, static_cast<int>(a.w), a3);
+      for (int t = 0; t < TM; ++t) {
+        if (t < tm) {
+          const uint4* xb = s_x + t * nblk + 4 * g;
+          int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 a = xb[j];
+            a0 = dp4a_us(pl[j][0], static_cast<int>(a.x), a0);
+            a1 = dp4a_us(pl[j][1], static_cast<int>(a.y), a1);
+            a2 = dp4a_us(pl[j][2], static_cast<int>(a.z), a2);
+            a3 = dp4a_us(pl[j][3], static_cast<int>(a.w), a3);
+          }
+          const int ag = a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6) - s_gs[t * G + g];
+          acc[t] = fma(gm, static_cast<double>(ag), acc[t]);   // the product is exact
         }
-        const int ag = a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6) - __ldcg(gsum + static_cast<size_t>(m) * G + g);
-        acc[t] = fma(gm, static_cast<double>(ag), acc[t]);   // the product is exact
       }
     }
   }
 #pragma unroll
-  for (int t = 0; t < MT; ++t) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-    const int m = m0 + t;
-    if (lane == 0 && m < M) y[static_cast<size_t>(m) * N + n] = __double2float_rn(acc[t] / static_cast<double>(__ldcg(scale + m)));
+  for (int t = 0; t < TM; ++t) s_part[(warp * kGRows + lane) * TM + t] = acc[t];
+  __syncthreads();
+  for (int i = tid; i < kGRows * tm; i += kGThreads) {
+    const int r = i / tm, t = i - r * tm;
+    const int nn = blockIdx.x * kGRows + r;
+    if (nn < N) {
+      double v = 0.0;
+      for (int sl = 0; sl < kGSlices; ++sl) v += s_part[(sl * kGRows + r) * TM + t];
+      y[static_cast<size_t>(m0 + t) * N + nn] = __double2float_rn(v / static_cast<double>(__ldcg(scale + m0 + t)));
+    }
   }
 }
 
@@ -379,9 +422,20 @@ cudaError_t launch_forward_grouped(const void* x, bool bf16, int M, int N, int K
                        : launch_pdl(bl_act_quant_grouped<float>, dim3(M), dim3(kGaThreads), 0, s,
                                     static_cast<const float*>(x), K, xt, gs, sc, xq_out, scale_out);
   if (e != cudaSuccess) return e;
-  const dim3 grid((N + kGfWarps - 1) / kGfWarps, M <= 1 ? 1 : (M + 3) / 4);
-  if (M <= 1) return launch_pdl(bl_gemv_grouped<1>, grid, dim3(kGfWarps * 32), 0, s, wp, gam, xt, gs, sc, y, M, N, K);
-  return launch_pdl(bl_gemv_grouped<4>, grid, dim3(kGfWarps * 32), 0, s, wp, gam, xt, gs, sc, y, M, N, K);
+  // token tile: as many tokens as M needs (1, 2, 4 or 8) while the staged codes fit
+  int tm = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+  while (tm > 1 && gemm_grouped_smem(K, tm) > kGMaxSmem) tm >>= 1;
+  const size_t smem = gemm_grouped_smem(K, tm);
+  const dim3 grid((N + kGRows - 1) / kGRows, (M + tm - 1) / tm);
+  auto go = [&](auto kern) -> cudaError_t {
+    const cudaError_t e2 = ensure_smem(reinterpret_cast<const void*>(kern), smem);
+    if (e2 != cudaSuccess) return e2;
+    return launch_pdl(kern, grid, dim3(kGThreads), smem, s, wp, gam, xt, gs, sc, y, M, N, K);
+  };
+  if (tm == 1) return go(bl_gemm_grouped<1>);
+  if (tm == 2) return go(bl_gemm_grouped<2>);
+  if (tm == 4) return go(bl_gemm_grouped<4>);
+  return go(bl_gemm_grouped<8>);
 }
 
 }  // namespace bl

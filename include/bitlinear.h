@@ -328,7 +328,7 @@ BL_API bl_status bitlinear_pack_weights_grouped(const float* W, int64_t N, int64
  *            bytes, 256-byte aligned; scratch. Calls that share a workspace
  *            must not overlap on the GPU.
  * Errors: as for bitlinear_forward, plus BL_ERR_INVALID_ARG for K % 64 != 0
- * and BL_ERR_UNSUPPORTED for M > 262140.
+ * and BL_ERR_UNSUPPORTED for M > 65535.
  * ------------------------------------------------------------------------- */
 BL_API size_t bitlinear_forward_grouped_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
