@@ -19,10 +19,11 @@
 // Layout of the table (int16, in shared memory): entry (nibble v, pair p)
 // with p = 8 w + q (packed word w of the row, nibble q of it) at index
 // (8 v + q) L + w, L = K/16 rounded up to a multiple of 64. In one read a
-// warp's lanes take words w = l + 32t at the same q: the lanes' entries lie
-// in consecutive 16-bit slots of one row of the table whatever their nibbles
-// are, because 8 v L is a multiple of 64 slots (32 banks), so the read is
-// free of bank conflicts. Nibble values above 10 never occur in packed data.
+// warp's lanes take words w = l + 32t at the same q, so lane l's entry sits
+// in bank (w / 2) mod 32 whatever its nibble v (8 v L is a multiple of 64
+// slots, 32 banks): lanes 2i and 2i + 1 share a bank, and a read costs one
+// wavefront when their nibbles agree and two when they differ. Nibble values
+// above 10 never occur in packed data.
 //
 // Per two weights the table form costs a shift, a mask, an address, a shared
 // load and an add; the dp4a form costs half an instruction per weight. It is

@@ -106,7 +106,9 @@ BL_DEVICE float group_gamma(const float4& v, int lane) {
       if (m[i]) t += static_cast<unsigned long long>(m[i]) << (f[i] - B);
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    return round_scaled_u64(t, B - 156);              // sum * 2^(B - 150) / 64
+    // sum * 2^(B - 150) / 64, rounded by the first lane of each half only
+    const float g = (lane & 15) == 0 ? round_scaled_u64(t, B - 156) : 0.f;
+    return __shfl_sync(0xffffffffu, g, lane & 16);
   }
   // rare: a weight more than 33 binades below the group's largest. Lane 0 of
   // each half adds the group's 64 weights into 288-bit fixed point.
@@ -202,7 +204,7 @@ cudaError_t launch_pack_grouped(const float* W, int64_t N, int64_t K, uint8_t* w
 
 namespace {
 
-constexpr int kGaThreads = 256;             // activation pass: one CTA per token
+constexpr int kGaThreads = 512;             // activation pass: one CTA per token
 constexpr int kGThreads = 256;              // contraction: 8 warps (k-slices) x 32 rows
 constexpr size_t kGMaxSmem = 200 * 1024;
 
@@ -358,9 +360,16 @@ bl_gemm_grouped(const uint8_t* __restrict__ wp, const float* __restrict__ gam, c
   if (n < N) {
     const uint4* wrow = reinterpret_cast<const uint4*>(wp + static_cast<size_t>(n) * (K >> 2));
     const float* grow = gam + static_cast<size_t>(n) * G;
+    // the next group's packed words and scale are loaded before this group's arithmetic
+    uint4 wn = warp < G ? __ldg(wrow + warp) : make_uint4(0u, 0u, 0u, 0u);
+    float gn = warp < G ? __ldg(grow + warp) : 0.f;
     for (int g = warp; g < G; g += kGSlices) {
-      const uint4 w = __ldg(wrow + g);
-      const double gm = static_cast<double>(__ldg(grow + g));
+      const uint4 w = wn;
+      const double gm = static_cast<double>(gn);
+      if (g + kGSlices < G) {
+        wn = __ldg(wrow + g + kGSlices);
+        gn = __ldg(grow + g + kGSlices);
+      }
       const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
       uint32_t pl[4][4];
 #pragma unroll
