@@ -228,6 +228,8 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
     const uint32_t lo = blockIdx.x * share;
     if (lo < xbytes) prefetch_l2(static_cast<const uint8_t*>(x) + lo, min(share, xbytes - lo));
   }
+  __shared__ int s_fail[1];                      // a contraction warp's weight wait gave up
+  if (tid == 0) s_fail[0] = 0;
   for (int i = tid; i < rows_pad * MT; i += kThreads) s_acc[i] = 0;
   pdl_wait();                                    // everything this grid reads is written and visible
   pdl_launch_dependents();
@@ -409,6 +411,7 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
   if (u < u_end) {
     // the CTA's rows are all needed: lane g waits for copy group g
     for (int g = lane; g < n_groups; g += 32) ok = mbar_wait_sleep(&s_bar[g], 0u) && ok;
+    if (!__all_sync(0xffffffffu, ok) && lane == 0) s_fail[0] = 1;
     __syncwarp();
     const uint32_t s_w32 = smem_u32(s_w) + 4u * lane;
     const uint32_t a32 = s_act32 + 16u * lane;
@@ -485,9 +488,10 @@ bl_gemv_dp4a(const uint8_t* __restrict__ wp, const void* __restrict__ x, const f
       }
     }
   }
-  // every bulk copy has landed before the CTA exits (a warp whose wait gave up
-  // left its copy in flight, and a CTA whose warps had no units never waited)
-  if (tid == 0)
+  // every bulk copy has landed before the CTA exits: each warp with units
+  // waited for every group, so only after a wait that gave up (its copy may
+  // still be in flight) does thread 0 wait again
+  if (tid == 0 && s_fail[0])
     for (int g = 0; g < n_groups; ++g) ok = mbar_wait_sleep(&s_bar[g], 0u) && ok;
   if (!ok) atomicExch(&g_dp4a_wait_error, 1);
 }
