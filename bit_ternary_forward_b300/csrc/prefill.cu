@@ -41,20 +41,20 @@
 //               the latency-bandwidth product of one SM's share of L2);
 //   warp 1      allocates 512 TMEM columns (two accumulators) and issues
 //               tcgen05.mma (M = 128 weight rows, N = BN tokens, K = 16)
-//               from one thread;
+//               from lane 0;
 //   warps 2..9  expand each packed stage into the fp16 operand, canonical
 //               128-byte-swizzled K-major layout, in a separate three-deep
-//               ring (half a row per thread);
+//               ring (half a row per thread), and arrive at the stage's
+//               named barrier, where the MMA warp syncs;
 //   warps 10..13 epilogue of the previous tile while the MMA fills the other
 //               accumulator: tcgen05.ld 32x32b (TMEM lane = weight row, one
 //               lane quarter per warp), stores coalesced along the rows.
-// Every wait on the full / expanded / empty stage barriers and on the
-// accumulator barriers is bounded. The expansion and epilogue warps sleep
+// Every wait on the full / empty stage barriers and on the accumulator
+// barriers is bounded; the named barriers are matched by construction (both
+// sides walk the same schedule). The expansion and epilogue warps sleep
 // until the phase completes instead of polling: polling warps take issue
-// slots from the MMA thread (measured 4-6 % slower). The two single threads
-// poll: the MMA thread on its expanded-stage barrier (1-3 % faster than
-// sleeping there, because its wake-up latency delays the next MMAs) and the
-// TMA producer on its free-stage barrier (no measurable difference).
+// slots from the MMA warp (measured 4-6 % slower). The TMA producer polls its
+// free-stage barrier (no measurable difference).
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -151,6 +151,13 @@ BL_DEVICE void umma_commit(uint64_t* bar) {
 BL_DEVICE void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+BL_DEVICE void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barriers 2 .. 2 + kEStages - 1: expanded buffer e is ready (the eight
+// expansion warps arrive, the MMA warp syncs; 288 threads).
+constexpr int kExpdBar = 2;
+constexpr int kExpdCount = 9 * 32;
 
 BL_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 BL_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -236,8 +243,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   uint8_t* misc = we_base + kEStages * kWeBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);            // TMA stage landed
   uint64_t* empty = full + kStages;                              // TMA stage consumed by the MMA
-  uint64_t* expd = empty + kStages;                              // expanded buffer ready
-  uint64_t* efree = expd + kEStages;                             // expanded buffer consumed
+  uint64_t* efree = empty + kStages;                             // expanded buffer consumed
   uint64_t* tfull = efree + kEStages;                            // accumulator b holds a finished tile
   uint64_t* tempty = tfull + 2;                                  // accumulator b has been read out
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
@@ -254,10 +260,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int e = 0; e < kEStages; ++e) {
-      mbar_init(&expd[e], 8);
-      mbar_init(&efree[e], 1);
-    }
+    for (int e = 0; e < kEStages; ++e) mbar_init(&efree[e], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
@@ -311,23 +314,25 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer
-    if (lane == 0) {
-      uint32_t g = 0, tcount = 0;
-      for (int item = 0; item < n_items; ++item, ++tcount) {
-        int tile, k0, k1;
-        sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
-        const uint32_t b = tcount & 1u;
-        if (tcount >= 2) ok = mbar_wait_sleep(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
+    // ---- MMA issuer: the whole warp runs the loop, lane 0 issues. It learns
+    // that an expanded stage is ready (which also means that its TMA stage
+    // has landed) at a named barrier, not by polling an mbarrier: a shared
+    // memory access by the thread right after its tcgen05.commit stalls for
+    // about 120 cycles, which at four MMAs per stage cost a fifth of the
+    // tensor pipe. The barrier cannot hang: the expansion warps arrive once
+    // for every stage of the same schedule, whatever their own waits return.
+    uint32_t g = 0, tcount = 0;
+    for (int item = 0; item < n_items; ++item, ++tcount) {
+      int tile, k0, k1;
+      sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
+      const uint32_t b = tcount & 1u;
+      if (tcount >= 2) ok = mbar_wait_sleep(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
+      const uint32_t d = tmem + b * 256u;
+      for (int it = k0; it < k1; ++it, ++g) {
+        const uint32_t s = g % kStages, e = g % kEStages;
+        named_bar(kExpdBar + static_cast<int>(e), kExpdCount);
         tc_fence_after();
-        const uint32_t d = tmem + b * 256u;
-        for (int it = k0; it < k1; ++it, ++g) {
-          const uint32_t s = g % kStages, e = g % kEStages, eph = (g / kEStages) & 1u;
-          // Polls (no suspend hint): the issuing thread's wake-up latency is on
-          // the tensor pipe's critical path; one polling lane costs the other
-          // warps little. Also means TMA stage s has landed.
-          ok = mbar_wait(&expd[e], eph) && ok;
-          tc_fence_after();
+        if (lane == 0) {
           const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes));   // activations [BN][64]
           const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
 #pragma unroll
@@ -336,8 +341,10 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           umma_commit(&empty[s]);
           umma_commit(&efree[e]);
         }
-        umma_commit(&tfull[b]);
+        __syncwarp();
       }
+      if (lane == 0) umma_commit(&tfull[b]);
+      __syncwarp();
     }
   } else if (warp < 10) {
     // ---- weight expansion: thread t expands half h = t / 128 (32 codes) of
@@ -368,8 +375,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           *reinterpret_cast<uint4*>(row + (((2u * q + 1u) ^ sw) << 4)) = c1;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&expd[e]);
+        named_arrive(kExpdBar + static_cast<int>(e), kExpdCount);
       }
     }
   } else {
