@@ -42,10 +42,11 @@
 //   warp 1      allocates 512 TMEM columns (two accumulators) and issues
 //               tcgen05.mma (M = 128 weight rows, N = BN tokens, K = 16)
 //               from lane 0;
-//   warps 2..9  expand each packed stage into the fp16 operand, canonical
-//               128-byte-swizzled K-major layout, in a separate three-deep
-//               ring (half a row per thread), and arrive at the stage's
-//               named barrier, where the MMA warp syncs;
+//   warps 2..9  expand each packed stage into the fp16 operand (half a row
+//               per thread) and arrive at the stage's named barrier, where
+//               the MMA warp syncs: into TMEM (tcgen05.st) for tiles of 128
+//               to 224 tokens, into a three-deep shared-memory ring in the
+//               canonical 128-byte-swizzled K-major layout for the others;
 //   warps 10..13 epilogue of the previous tile while the MMA fills the other
 //               accumulator: tcgen05.ld 32x32b (TMEM lane = weight row, one
 //               lane quarter per warp), stores coalesced along the rows.
@@ -83,19 +84,37 @@ constexpr uint32_t kWeBytes = kBM * kBK * 2;    // 16384
 constexpr uint32_t kEpiBytes = 3 * kMaxBN * 4 + 64;
 constexpr uint32_t kMiscBytes = 256 + 2 * kEpiBytes;
 constexpr uint32_t kSmemBudget = 232448;    // opt-in shared memory per CTA
+// Where the expanded weights (the MMA's A operand) live. Tiles of 128 to 224
+// tokens keep them in tensor memory: their two accumulators (columns
+// [0, BN) and [256, 256 + BN)) leave 32-column slots at the top of each
+// 256-column half, one 64-k stage of 128 rows x 64 fp16 each. The expansion
+// warps write them with tcgen05.st, which the MMA may read right after the
+// handoff. Weights written to shared memory instead need a generic-to-async
+// proxy fence before the MMA reads them, and that fence, issued while MMAs
+// are in flight, costs the tensor pipe about 40 % (measured: 225 against 128
+// cycles per 128 x 256 x 16 MMA with the stage handoff alone). The 256-token
+// tile, whose accumulators fill the 512 columns, and the 32- and 64-token
+// tiles keep the shared-memory ring.
+constexpr bool ts_for(int bn) { return bn >= 128 && bn <= 224; }
+constexpr int a_stages(int bn) { return 2 * ((256 - bn) / 32) < 4 ? 2 * ((256 - bn) / 32) : 4; }
+constexpr int e_stages(int bn) { return ts_for(bn) ? a_stages(bn) : kEStages; }
+constexpr uint32_t we_ring_bytes(int bn) { return ts_for(bn) ? 0u : kEStages * kWeBytes; }
 // TMA stage: activation tile [BN][64] fp16, then packed weights [128][16] bytes
 // (a multiple of 1024 bytes, so every swizzled tile stays 1024-aligned).
 constexpr uint32_t stage_bytes(int bn) { return static_cast<uint32_t>(bn) * kBK * 2 + kWpBytes; }
 // As many TMA stages as fit: the ring should hold about one latency's worth
 // of the SM's operand stream whatever the tile width.
 constexpr int stages_for(int bn) {
-  return static_cast<int>((kSmemBudget - 1024 - kEStages * kWeBytes - kMiscBytes) / stage_bytes(bn)) < kMaxStages
-             ? static_cast<int>((kSmemBudget - 1024 - kEStages * kWeBytes - kMiscBytes) / stage_bytes(bn))
+  return static_cast<int>((kSmemBudget - 1024 - we_ring_bytes(bn) - kMiscBytes) / stage_bytes(bn)) < kMaxStages
+             ? static_cast<int>((kSmemBudget - 1024 - we_ring_bytes(bn) - kMiscBytes) / stage_bytes(bn))
              : kMaxStages;
 }
 constexpr uint32_t smem_for(int bn) {
-  return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + kEStages * kWeBytes + kMiscBytes + 1024;
+  return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + we_ring_bytes(bn) + kMiscBytes + 1024;
 }
+// barriers: full and empty per TMA stage, efree per expanded stage, tfull and
+// tempty per accumulator, then the TMEM base and a flag
+static_assert(8 * (2 * kMaxStages + 4 + 4) + 8 <= 256, "barrier area");
 __device__ int g_tc_wait_error;
 
 // L2 prefetch of one box of a tensor map.
@@ -143,6 +162,19 @@ BL_DEVICE void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_
       : "memory");
 }
 
+// The same with the A operand (the weights, 128 rows x 16 k of fp16) read
+// from tensor memory: lane = row, two consecutive k per 32-bit column, the
+// lower k in the low half.
+template <int BN>
+BL_DEVICE void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc_f16<BN>()), "r"(accumulate)
+      : "memory");
+}
+
 BL_DEVICE void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -154,7 +186,7 @@ BL_DEVICE void named_bar(int id, int count) {
 BL_DEVICE void named_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// Named barriers 2 .. 2 + kEStages - 1: expanded buffer e is ready (the eight
+// Named barriers 2 .. 2 + e_stages(BN) - 1 (at most 2 .. 5): expanded stage e is ready (the eight
 // expansion warps arrive, the MMA warp syncs; 288 threads).
 constexpr int kExpdBar = 2;
 constexpr int kExpdCount = 9 * 32;
@@ -172,6 +204,26 @@ BL_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Stores 16 consecutive 32-bit columns of this thread's TMEM lane and waits
+// until they are written.
+BL_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// TMEM column of expanded weight stage e (0 <= e < a_stages(BN)): the free
+// columns at the top of each accumulator's 256-column half.
+template <int BN>
+BL_DEVICE uint32_t a_col(uint32_t e) {
+  constexpr uint32_t kHalf = a_stages(BN) >= 2 ? static_cast<uint32_t>(a_stages(BN) / 2) : 1u;
+  return (e / kHalf) * 256u + (256u - 32u * kHalf) + 32u * (e % kHalf);
 }
 
 }  // namespace
@@ -237,14 +289,16 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   constexpr int kStages = stages_for(BN);
   constexpr uint32_t kStageBytes = stage_bytes(BN);
   constexpr uint32_t kXBytes = static_cast<uint32_t>(BN) * kBK * 2;
+  constexpr bool kTS = ts_for(BN);               // expanded weights in TMEM
+  constexpr int kES = e_stages(BN);              // expanded-weight stages
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* we_base = smem + kStages * kStageBytes;               // expanded weights, 1024-aligned
-  uint8_t* misc = we_base + kEStages * kWeBytes;
+  uint8_t* we_base = smem + kStages * kStageBytes;               // expanded weights, 1024-aligned (not kTS)
+  uint8_t* misc = we_base + we_ring_bytes(BN);
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);            // TMA stage landed
   uint64_t* empty = full + kStages;                              // TMA stage consumed by the MMA
   uint64_t* efree = empty + kStages;                             // expanded buffer consumed
-  uint64_t* tfull = efree + kEStages;                            // accumulator b holds a finished tile
+  uint64_t* tfull = efree + kES;                                 // accumulator b holds a finished tile
   uint64_t* tempty = tfull + 2;                                  // accumulator b has been read out
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 1);         // this CTA completes a split tile
@@ -260,7 +314,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int e = 0; e < kEStages; ++e) mbar_init(&efree[e], 1);
+    for (int e = 0; e < kES; ++e) mbar_init(&efree[e], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
@@ -329,15 +383,22 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (tcount >= 2) ok = mbar_wait_sleep(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
       const uint32_t d = tmem + b * 256u;
       for (int it = k0; it < k1; ++it, ++g) {
-        const uint32_t s = g % kStages, e = g % kEStages;
+        const uint32_t s = g % kStages, e = g % kES;
         named_bar(kExpdBar + static_cast<int>(e), kExpdCount);
         tc_fence_after();
         if (lane == 0) {
           const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes));   // activations [BN][64]
-          const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
+          if constexpr (kTS) {
+            const uint32_t a = tmem + a_col<BN>(e);                             // weights, TMEM lanes 0..127
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_f16<BN>(d, adesc + 2u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_f16_ts<BN>(d, a + 8u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
+          } else {
+            const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_f16<BN>(d, adesc + 2u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
+          }
           umma_commit(&empty[s]);
           umma_commit(&efree[e]);
         }
@@ -346,7 +407,46 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (lane == 0) umma_commit(&tfull[b]);
       __syncwarp();
     }
-  } else if (warp < 10) {
+  } else if (warp < 10 && kTS) {
+    // ---- weight expansion into TMEM: warp w reaches TMEM lanes 32 (w % 4) ..
+    // 32 (w % 4) + 31 only, so lane l expands row 32 (w % 4) + l; warps 2..5
+    // take half h = 0 of the stage (32 codes, 16 columns), warps 6..9 h = 1.
+    const int quarter = warp & 3, h = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 16u * static_cast<uint32_t>(h);
+    uint32_t g = 0;
+    for (int item = 0; item < n_items; ++item) {
+      int tile, k0, k1;
+      sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
+      for (int it = k0; it < k1; ++it, ++g) {
+        const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
+        const uint32_t e = g % kES, eph = (g / kES) & 1u;
+        ok = mbar_wait_sleep(&full[s], ph) && ok;
+        if (g >= static_cast<uint32_t>(kES)) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
+        tc_fence_after();
+        const uint2 pw = *reinterpret_cast<const uint2*>(smem + s * kStageBytes + kXBytes + r * 16 + h * 8);
+        const uint32_t words[2] = {pw.x, pw.y};
+        uint32_t v[16];
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          // column 8 q' + c of this half holds slots 16 q' + 2c (low) and 16 q' + 2c + 1
+          const uint32_t lo = __byte_perm(words[qq], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
+          const uint32_t hi = __byte_perm(words[qq], 0u, 0x4342);   // bytes 2, 3
+          v[8 * qq + 0] = lo & 0x00030003u;
+          v[8 * qq + 1] = hi & 0x00030003u;
+          v[8 * qq + 2] = lo & 0x000c000cu;
+          v[8 * qq + 3] = hi & 0x000c000cu;
+          v[8 * qq + 4] = lo & 0x00300030u;
+          v[8 * qq + 5] = hi & 0x00300030u;
+          v[8 * qq + 6] = lo & 0x00c000c0u;
+          v[8 * qq + 7] = hi & 0x00c000c0u;
+        }
+        tmem_st16(lane_base + a_col<BN>(e), v);
+        tc_fence_before();
+        named_arrive(kExpdBar + static_cast<int>(e), kExpdCount);
+      }
+    }
+  } else if (warp < 10 && !kTS) {
     // ---- weight expansion: thread t expands half h = t / 128 (32 codes) of
     // row r = t % 128 of each stage
     const int t = tid - 64;
@@ -358,9 +458,9 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
       for (int it = k0; it < k1; ++it, ++g) {
         const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
-        const uint32_t e = g % kEStages, eph = (g / kEStages) & 1u;
+        const uint32_t e = g % kES, eph = (g / kES) & 1u;
         ok = mbar_wait_sleep(&full[s], ph) && ok;
-        if (g >= kEStages) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
+        if (g >= static_cast<uint32_t>(kES)) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
         const uint2 pw = *reinterpret_cast<const uint2*>(smem + s * kStageBytes + kXBytes + r * 16 + h * 8);
         uint8_t* row = we_base + e * kWeBytes + r * 128;
         const uint32_t words[2] = {pw.x, pw.y};
@@ -728,19 +828,26 @@ EncodeTiled encode_fn() {
 
 }  // namespace
 
+// Time of one k-stage of a tile relative to the 256-token tile, measured on
+// B300 at M = 2048 over the 2B and 7B projection shapes: the tiles whose
+// weights live in TMEM (128 to 224 tokens) take 0.67-0.76 of the 256-token
+// tile's stage, whose weights go through shared memory; the 32- and 64-token
+// tiles keep the earlier estimate.
+constexpr double stage_cost(int bn) {
+  return bn == 256 ? 1.0 : bn == 224 ? 0.76 : bn == 192 ? 0.72 : bn == 160 ? 0.70 : bn == 128 ? 0.67 : 0.78;
+}
+
 // Launch plan: token-tile width BN, grid and work split. For each BN the
 // tiles are dealt round-robin to the SMs; a last round that would occupy at
 // most a tenth of the SMs is split by k-stages instead (stream-K), costed as
-// the fraction of a round it fills plus 5% for the buffer traffic. (Every
-// contributing CTA adds a whole 128 x BN fp32 partial with atomics; with more
-// split tiles that traffic costs more than the idle SMs it saves.) A narrow
-// tile that holds every token (M <= BN <= 64) has small partials, so when
-// there are fewer such tiles than SMs they are always split.
-// A k-stage costs nearly the same for narrow tiles (the per-stage issue work
-// of the MMA thread, not the tensor pipe, sets its length there), so a
-// tile's time is taken as proportional to max(BN, 200); among equal costs the
-// plan with fewer token tiles, then the narrower tile, wins (a narrower stage
-// leaves room for more of them in shared memory).
+// the fraction of a round it fills plus a fixed 12 k-stages for the partial
+// sums and the final epilogue. (Every contributing CTA adds a whole 128 x BN
+// fp32 partial with atomics; with more split tiles that traffic costs more
+// than the idle SMs it saves.) A narrow tile that holds every token
+// (M <= BN <= 64) has small partials, so when there are fewer such tiles
+// than SMs they are always split. A plan's cost is its rounds times
+// stage_cost(BN); among equal costs the plan with fewer token tiles, then
+// the narrower tile, wins.
 TcPlan tc_plan(int M, int N, int K, int sms) {
   const int cands[7] = {256, 224, 192, 160, 128, 64, 32};
   const int tn = (N + kBM - 1) / kBM;
@@ -753,8 +860,9 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
     const int tiles = tn * tm;
     const int full = tiles / sms, r = tiles % sms;
     const bool sk = r > 0 && (10 * r <= sms || (full == 0 && bn <= 64 && tm == 1));
-    const double rounds = r == 0 ? full : (sk ? full + static_cast<double>(r) / sms + 0.05 : full + 1.0);
-    const double cost = rounds * (bn > 200 ? bn : 200);
+    const double rounds =
+        r == 0 ? full : (sk ? full + static_cast<double>(r) / sms + 12.0 / k_iters : full + 1.0);
+    const double cost = rounds * stage_cost(bn);
     if (best_cost >= 0.0 && (cost > best_cost || (cost == best_cost && tm > best_tm))) continue;
     best_cost = cost;
     best_tm = tm;
