@@ -39,17 +39,21 @@
 //               swizzle) and packed weight tile [128][16] bytes per stage,
 //               as many stages as fit (5 at BN = 256, 10 at BN = 128: about
 //               the latency-bandwidth product of one SM's share of L2);
-//   warp 1      allocates 512 TMEM columns (two accumulators) and issues
-//               tcgen05.mma (M = 128 weight rows, N = BN tokens, K = 16)
-//               from lane 0;
+//   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma
+//               (M = 128 weight rows, N = BN tokens, K = 16) from lane 0;
+//               TMEM holds two accumulators (and, from 128 to 224 tokens,
+//               expanded weight stages beside them), or for the 256-token
+//               tile one accumulator and four weight stages;
 //   warps 2..9  expand each packed stage into the fp16 operand (half a row
 //               per thread) and arrive at the stage's named barrier, where
 //               the MMA warp syncs: into TMEM (tcgen05.st) for tiles of 128
-//               to 224 tokens, into a three-deep shared-memory ring in the
-//               canonical 128-byte-swizzled K-major layout for the others;
+//               to 256 tokens, into a three-deep shared-memory ring in the
+//               canonical 128-byte-swizzled K-major layout for the 32- and
+//               64-token tiles;
 //   warps 10..13 epilogue of the previous tile while the MMA fills the other
-//               accumulator: tcgen05.ld 32x32b (TMEM lane = weight row, one
-//               lane quarter per warp), stores coalesced along the rows.
+//               accumulator (with one accumulator the MMA waits for it):
+//               tcgen05.ld 32x32b (TMEM lane = weight row, one lane quarter
+//               per warp), stores coalesced along the rows.
 // Every wait on the full / empty stage barriers and on the accumulator
 // barriers is bounded; the named barriers are matched by construction (both
 // sides walk the same schedule). The expansion and epilogue warps sleep
@@ -84,19 +88,25 @@ constexpr uint32_t kWeBytes = kBM * kBK * 2;    // 16384
 constexpr uint32_t kEpiBytes = 3 * kMaxBN * 4 + 64;
 constexpr uint32_t kMiscBytes = 256 + 2 * kEpiBytes;
 constexpr uint32_t kSmemBudget = 232448;    // opt-in shared memory per CTA
-// Where the expanded weights (the MMA's A operand) live. Tiles of 128 to 224
-// tokens keep them in tensor memory: their two accumulators (columns
-// [0, BN) and [256, 256 + BN)) leave 32-column slots at the top of each
-// 256-column half, one 64-k stage of 128 rows x 64 fp16 each. The expansion
+// Where the expanded weights (the MMA's A operand) live. Tiles of 128 to 256
+// tokens keep them in tensor memory, in 32-column slots of one 64-k stage
+// (128 rows x 64 fp16) each: from 128 to 224 tokens at the top of each
+// 256-column half, beside two accumulators (columns [0, BN) and
+// [256, 256 + BN)); at 256 tokens in the upper half, beside one. The expansion
 // warps write them with tcgen05.st, which the MMA may read right after the
 // handoff. Weights written to shared memory instead need a generic-to-async
 // proxy fence before the MMA reads them, and that fence, issued while MMAs
 // are in flight, costs the tensor pipe about 40 % (measured: 225 against 128
-// cycles per 128 x 256 x 16 MMA with the stage handoff alone). The 256-token
-// tile, whose accumulators fill the 512 columns, and the 32- and 64-token
-// tiles keep the shared-memory ring.
-constexpr bool ts_for(int bn) { return bn >= 128 && bn <= 224; }
-constexpr int a_stages(int bn) { return 2 * ((256 - bn) / 32) < 4 ? 2 * ((256 - bn) / 32) : 4; }
+// cycles per 128 x 256 x 16 MMA with the stage handoff alone). The 32- and
+// 64-token tiles keep the shared-memory ring.
+constexpr bool ts_for(int bn) { return bn >= 128 && bn <= 256; }
+// accumulators in TMEM: two (the MMA fills one while the epilogue drains the
+// other), except for the 256-token tile with its weights in TMEM, whose one
+// accumulator takes [0, 256) and leaves [256, 512) to the weight stages
+constexpr int acc_bufs(int bn) { return bn == 256 ? 1 : 2; }
+constexpr int a_stages(int bn) {
+  return bn == 256 ? 4 : (2 * ((256 - bn) / 32) < 4 ? 2 * ((256 - bn) / 32) : 4);
+}
 constexpr int e_stages(int bn) { return ts_for(bn) ? a_stages(bn) : kEStages; }
 constexpr uint32_t we_ring_bytes(int bn) { return ts_for(bn) ? 0u : kEStages * kWeBytes; }
 // TMA stage: activation tile [BN][64] fp16, then packed weights [128][16] bytes
@@ -219,9 +229,11 @@ BL_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
 }
 
 // TMEM column of expanded weight stage e (0 <= e < a_stages(BN)): the free
-// columns at the top of each accumulator's 256-column half.
+// columns at the top of each accumulator's 256-column half, or the upper half
+// when one accumulator takes the lower.
 template <int BN>
 BL_DEVICE uint32_t a_col(uint32_t e) {
+  if constexpr (acc_bufs(BN) == 1) return 256u + 32u * e;
   constexpr uint32_t kHalf = a_stages(BN) >= 2 ? static_cast<uint32_t>(a_stages(BN) / 2) : 1u;
   return (e / kHalf) * 256u + (256u - 32u * kHalf) + 32u * (e % kHalf);
 }
@@ -290,6 +302,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   constexpr uint32_t kStageBytes = stage_bytes(BN);
   constexpr uint32_t kXBytes = static_cast<uint32_t>(BN) * kBK * 2;
   constexpr bool kTS = ts_for(BN);               // expanded weights in TMEM
+  constexpr uint32_t kAcc = kTS ? acc_bufs(BN) : 2u;   // TMEM accumulators
   constexpr int kES = e_stages(BN);              // expanded-weight stages
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -379,8 +392,9 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     for (int item = 0; item < n_items; ++item, ++tcount) {
       int tile, k0, k1;
       sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
-      const uint32_t b = tcount & 1u;
-      if (tcount >= 2) ok = mbar_wait_sleep(&tempty[b], ((tcount >> 1) & 1u) ^ 1u) && ok;
+      // accumulator b's use u of this tile waits for the epilogue of use u - 1
+      const uint32_t b = tcount % kAcc, u = tcount / kAcc;
+      if (u >= 1) ok = mbar_wait_sleep(&tempty[b], (u & 1u) ^ 1u) && ok;
       const uint32_t d = tmem + b * 256u;
       for (int it = k0; it < k1; ++it, ++g) {
         const uint32_t s = g % kStages, e = g % kES;
@@ -500,7 +514,8 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       int tile, k0, k1;
       sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
       const int n0 = (tile % n_tiles_n) * kBM, m0 = (tile / n_tiles_n) * BN;
-      const uint32_t b = tcount & 1u;
+      const uint32_t b = tcount & 1u;               // per-token data buffer
+      const uint32_t bacc = tcount % kAcc;          // accumulator
       float* s_scale = reinterpret_cast<float*>(misc + 256 + b * kEpiBytes);
       float* s_rcp = s_scale + kMaxBN;           // recip_for_div(s): fp32(1/s), or 0 outside 2^-96..2^96
       float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q as (exact) fp32
@@ -527,7 +542,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (lane == 0) s_fast[c] = fast;
       }
       named_bar(1, 128);                         // the per-token data is complete
-      ok = mbar_wait_sleep(&tfull[b], (tcount >> 1) & 1u) && ok;
+      ok = mbar_wait_sleep(&tfull[bacc], (tcount / kAcc) & 1u) && ok;
       tc_fence_after();
       const int n = n0 + quarter * 32 + lane;
       float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
@@ -569,7 +584,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + b * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+          tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
           if (n >= N) continue;
           float dv[32];
 #pragma unroll
@@ -578,7 +593,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
+        if (lane == 0) mbar_arrive(&tempty[bacc]);
       } else {
         // part of a split tile: add the partial into the tile's buffer
         // [token][row]; the 32 lanes of a warp add 32 consecutive floats
@@ -588,7 +603,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + b * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+          tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
           if (n >= N) continue;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -596,7 +611,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[b]);
+        if (lane == 0) mbar_arrive(&tempty[bacc]);
         // the CTA whose stages complete the tile's k-count writes it
         __threadfence();
         named_bar(1, 128);
@@ -828,13 +843,13 @@ EncodeTiled encode_fn() {
 
 }  // namespace
 
-// Time of one k-stage of a tile relative to the 256-token tile, measured on
-// B300 at M = 2048 over the 2B and 7B projection shapes: the tiles whose
-// weights live in TMEM (128 to 224 tokens) take 0.67-0.76 of the 256-token
-// tile's stage, whose weights go through shared memory; the 32- and 64-token
-// tiles keep the earlier estimate.
+// Time of one k-stage of a tile, in units of the 256-token stage with the
+// weights in shared memory, measured on B300 over the 2B and 7B projection
+// shapes at M = 512-2048. The tiles with their weights in TMEM take 0.62
+// (256 tokens, one accumulator, its epilogue not overlapped) to 0.76; the
+// 32- and 64-token tiles keep the earlier estimate.
 constexpr double stage_cost(int bn) {
-  return bn == 256 ? 1.0 : bn == 224 ? 0.76 : bn == 192 ? 0.72 : bn == 160 ? 0.70 : bn == 128 ? 0.67 : 0.78;
+  return bn == 256 ? 0.62 : bn == 224 ? 0.76 : bn == 192 ? 0.72 : bn == 160 ? 0.70 : bn == 128 ? 0.67 : 0.78;
 }
 
 // Launch plan: token-tile width BN, grid and work split. For each BN the
@@ -856,6 +871,9 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   double best_cost = -1.0;
   int best_tm = 0;
   for (int bn : cands) {
+    // the 256-token tile's epilogue holds its one accumulator, so it needs
+    // tiles long in k and nearly full in tokens
+    if (bn == 256 && (M <= 192 || k_iters < 16)) continue;
     const int tm = (M + bn - 1) / bn;
     const int tiles = tn * tm;
     const int full = tiles / sms, r = tiles % sms;
