@@ -37,23 +37,25 @@
 // epilogue from the buffer. The roles:
 //   warp 0      TMA producer: activation tile [BN][64] fp16 (128-byte
 //               swizzle) and packed weight tile [128][16] bytes per stage,
-//               as many stages as fit (5 at BN = 256, 10 at BN = 128: about
+//               as many stages as fit (6 at BN = 256, 10 at BN = 128: about
 //               the latency-bandwidth product of one SM's share of L2);
 //   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma
 //               (M = 128 weight rows, N = BN tokens, K = 16) from lane 0;
 //               TMEM holds two accumulators (and, from 128 to 224 tokens,
 //               expanded weight stages beside them), or for the 256-token
 //               tile one accumulator and four weight stages;
-//   warps 2..9  expand each packed stage into the fp16 operand (half a row
-//               per thread) and arrive at the stage's named barrier, where
-//               the MMA warp syncs: into TMEM (tcgen05.st) for tiles of 128
-//               to 256 tokens, into a three-deep shared-memory ring in the
-//               canonical 128-byte-swizzled K-major layout for the 32- and
-//               64-token tiles;
-//   warps 10..13 epilogue of the previous tile while the MMA fills the other
-//               accumulator (with one accumulator the MMA waits for it):
-//               tcgen05.ld 32x32b (TMEM lane = weight row, one lane quarter
-//               per warp), stores coalesced along the rows.
+//   warps 2..5  expand each packed stage into the fp16 operand (a row per
+//               thread; warp w holds TMEM lanes 32 (w % 4) ..) and arrive at
+//               the stage's named barrier, where the MMA warp syncs: into
+//               TMEM (tcgen05.st) for tiles of 128 to 256 tokens, into a
+//               three-deep shared-memory ring in the canonical
+//               128-byte-swizzled K-major layout for the 32- and 64-token
+//               tiles;
+//   warps 6..13 epilogue of the previous tile while the MMA fills the other
+//               accumulator (with one accumulator the MMA waits for it, so
+//               two warps share each TMEM lane quarter, taking alternate
+//               32-token chunks): tcgen05.ld 32x32b (TMEM lane = weight
+//               row), stores coalesced along the rows.
 // Every wait on the full / empty stage barriers and on the accumulator
 // barriers is bounded; the named barriers are matched by construction (both
 // sides walk the same schedule). The expansion and epilogue warps sleep
@@ -76,7 +78,11 @@ namespace {
 constexpr int kBM = 128;                    // weight rows per tile: the MMA's M
 constexpr int kBK = 64;                     // k per stage (one 128-byte fp16 swizzle atom)
 constexpr int kEStages = 3;                 // expanded-weight ring
-constexpr int kThreads = 448;
+constexpr int kExpWarps = 4;                 // expansion: one warp per TMEM lane quarter, a row per thread
+constexpr int kEpiWarps = 8;                 // epilogue: two warps per TMEM lane quarter
+constexpr int kEpiWarp0 = 2 + kExpWarps;     // first epilogue warp
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);   // producer, MMA, expansion, epilogue
 constexpr int kMaxBN = 256;                 // tokens per tile at most: the MMA's N
 constexpr int kMaxStages = 10;
 constexpr int kPrefetchStages = 32;         // weight boxes a CTA prefetches into L2 before its dependency wait
@@ -196,10 +202,10 @@ BL_DEVICE void named_bar(int id, int count) {
 BL_DEVICE void named_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// Named barriers 2 .. 2 + e_stages(BN) - 1 (at most 2 .. 5): expanded stage e is ready (the eight
-// expansion warps arrive, the MMA warp syncs; 288 threads).
+// Named barriers 2 .. 2 + e_stages(BN) - 1 (at most 2 .. 5): expanded stage e
+// is ready (the expansion warps arrive, the MMA warp syncs).
 constexpr int kExpdBar = 2;
-constexpr int kExpdCount = 9 * 32;
+constexpr int kExpdCount = 32 * (kExpWarps + 1);
 
 BL_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 BL_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -216,14 +222,16 @@ BL_DEVICE void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Stores 16 consecutive 32-bit columns of this thread's TMEM lane and waits
+// Stores 32 consecutive 32-bit columns of this thread's TMEM lane and waits
 // until they are written.
-BL_DEVICE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+BL_DEVICE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -330,7 +338,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     for (int e = 0; e < kES; ++e) mbar_init(&efree[e], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], kEpiWarps);
     }
     mbar_init_fence();
   }
@@ -421,13 +429,13 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (lane == 0) umma_commit(&tfull[b]);
       __syncwarp();
     }
-  } else if (warp < 10 && kTS) {
+  } else if (warp < kEpiWarp0 && kTS) {
     // ---- weight expansion into TMEM: warp w reaches TMEM lanes 32 (w % 4) ..
-    // 32 (w % 4) + 31 only, so lane l expands row 32 (w % 4) + l; warps 2..5
-    // take half h = 0 of the stage (32 codes, 16 columns), warps 6..9 h = 1.
-    const int quarter = warp & 3, h = (warp - 2) >> 2;
+    // 32 (w % 4) + 31 only, so lane l expands row 32 (w % 4) + l, all 64
+    // codes of the stage (32 columns).
+    const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 16u * static_cast<uint32_t>(h);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t g = 0;
     for (int item = 0; item < n_items; ++item) {
       int tile, k0, k1;
@@ -438,33 +446,31 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         ok = mbar_wait_sleep(&full[s], ph) && ok;
         if (g >= static_cast<uint32_t>(kES)) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
         tc_fence_after();
-        const uint2 pw = *reinterpret_cast<const uint2*>(smem + s * kStageBytes + kXBytes + r * 16 + h * 8);
-        const uint32_t words[2] = {pw.x, pw.y};
-        uint32_t v[16];
+        const uint4 pw = *reinterpret_cast<const uint4*>(smem + s * kStageBytes + kXBytes + r * 16);
+        const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
+        uint32_t v[32];
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          // column 8 q' + c of this half holds slots 16 q' + 2c (low) and 16 q' + 2c + 1
-          const uint32_t lo = __byte_perm(words[qq], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
-          const uint32_t hi = __byte_perm(words[qq], 0u, 0x4342);   // bytes 2, 3
-          v[8 * qq + 0] = lo & 0x00030003u;
-          v[8 * qq + 1] = hi & 0x00030003u;
-          v[8 * qq + 2] = lo & 0x000c000cu;
-          v[8 * qq + 3] = hi & 0x000c000cu;
-          v[8 * qq + 4] = lo & 0x00300030u;
-          v[8 * qq + 5] = hi & 0x00300030u;
-          v[8 * qq + 6] = lo & 0x00c000c0u;
-          v[8 * qq + 7] = hi & 0x00c000c0u;
+        for (int q = 0; q < 4; ++q) {
+          // column 8 q + c holds slots 16 q + 2c (low half) and 16 q + 2c + 1
+          const uint32_t lo = __byte_perm(words[q], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
+          const uint32_t hi = __byte_perm(words[q], 0u, 0x4342);   // bytes 2, 3
+          v[8 * q + 0] = lo & 0x00030003u;
+          v[8 * q + 1] = hi & 0x00030003u;
+          v[8 * q + 2] = lo & 0x000c000cu;
+          v[8 * q + 3] = hi & 0x000c000cu;
+          v[8 * q + 4] = lo & 0x00300030u;
+          v[8 * q + 5] = hi & 0x00300030u;
+          v[8 * q + 6] = lo & 0x00c000c0u;
+          v[8 * q + 7] = hi & 0x00c000c0u;
         }
-        tmem_st16(lane_base + a_col<BN>(e), v);
+        tmem_st32(lane_base + a_col<BN>(e), v);
         tc_fence_before();
         named_arrive(kExpdBar + static_cast<int>(e), kExpdCount);
       }
     }
-  } else if (warp < 10 && !kTS) {
-    // ---- weight expansion: thread t expands half h = t / 128 (32 codes) of
-    // row r = t % 128 of each stage
-    const int t = tid - 64;
-    const int r = t & (kBM - 1), h = t >> 7;
+  } else if (warp < kEpiWarp0 && !kTS) {
+    // ---- weight expansion: thread r expands row r of each stage (64 codes)
+    const int r = tid - 64;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
     uint32_t g = 0;
     for (int item = 0; item < n_items; ++item) {
@@ -475,14 +481,13 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         const uint32_t e = g % kES, eph = (g / kES) & 1u;
         ok = mbar_wait_sleep(&full[s], ph) && ok;
         if (g >= static_cast<uint32_t>(kES)) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
-        const uint2 pw = *reinterpret_cast<const uint2*>(smem + s * kStageBytes + kXBytes + r * 16 + h * 8);
+        const uint4 pw = *reinterpret_cast<const uint4*>(smem + s * kStageBytes + kXBytes + r * 16);
         uint8_t* row = we_base + e * kWeBytes + r * 128;
-        const uint32_t words[2] = {pw.x, pw.y};
+        const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
 #pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const uint32_t q = static_cast<uint32_t>(2 * h + qq);
-          const uint32_t lo = __byte_perm(words[qq], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
-          const uint32_t hi = __byte_perm(words[qq], 0u, 0x4342);   // bytes 2, 3
+        for (uint32_t q = 0; q < 4; ++q) {
+          const uint32_t lo = __byte_perm(words[q], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
+          const uint32_t hi = __byte_perm(words[q], 0u, 0x4342);   // bytes 2, 3
           const uint4 c0 = make_uint4(lo & 0x00030003u, hi & 0x00030003u, lo & 0x000c000cu, hi & 0x000c000cu);
           const uint4 c1 = make_uint4(lo & 0x00300030u, hi & 0x00300030u, lo & 0x00c000c0u, hi & 0x00c000c0u);
           *reinterpret_cast<uint4*>(row + (((2u * q) ^ sw) << 4)) = c0;
@@ -505,8 +510,10 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     // 2^-96..2^96 and 2^24 gamma max(1/s) < 2^125 and gamma min(1/s) > 2^-99
     // (no quotient can leave the normal range). Other chunks take
     // div_rn_recip, which checks each output.
-    const int et = tid - 320;                    // 0..127
+    const int et = tid - 32 * kEpiWarp0;         // 0 .. kEpiThreads - 1
     const int quarter = warp & 3;
+    // the two warps of a lane quarter take alternate 32-token chunks of each tile
+    const int chunk0 = 32 * ((warp - kEpiWarp0) >> 2);
     const float gm = OUT_ACC ? 0.f : __ldg(gamma);
     const bool gamma_fast = OUT_ACC || (gm > 0x1p-72f && gm < 0x1p72f);
     uint32_t tcount = 0;
@@ -520,14 +527,14 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       float* s_rcp = s_scale + kMaxBN;           // recip_for_div(s): fp32(1/s), or 0 outside 2^-96..2^96
       float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q as (exact) fp32
       int* s_fast = reinterpret_cast<int*>(s_rowsum + kMaxBN);   // per 32-token chunk: the branch-free form is exact
-      for (int i = et; i < BN; i += 128) {
+      for (int i = et; i < BN; i += kEpiThreads) {
         const int m = m0 + i;
         const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
         s_scale[i] = sc;
         s_rcp[i] = recip_for_div(sc);
         s_rowsum[i] = static_cast<float>(m < M ? __ldg(rowsum + m) : 0);   // |sum| <= 128 K <= 2^23: exact
       }
-      for (int c = warp - 10; c < BN / 32; c += 4) {
+      for (int c = warp - kEpiWarp0; c < BN / 32; c += kEpiWarps) {
         const int m = m0 + c * 32 + lane;
         const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
         const float r = recip_for_div(sc);
@@ -541,7 +548,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
                                       __fmul_rn(gm, rmin) > 0x1p-99f);
         if (lane == 0) s_fast[c] = fast;
       }
-      named_bar(1, 128);                         // the per-token data is complete
+      named_bar(1, kEpiThreads);                 // the per-token data is complete
       ok = mbar_wait_sleep(&tfull[bacc], (tcount / kAcc) & 1u) && ok;
       tc_fence_after();
       const int n = n0 + quarter * 32 + lane;
@@ -582,7 +589,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (tile < sch.dp_tiles) {
         // a whole tile: straight from TMEM
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = chunk0; c0 < BN; c0 += 64) {
           uint32_t v[32];
           tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
           if (n >= N) continue;
@@ -601,7 +608,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         float* buf = sk_buf + static_cast<size_t>(sk) * BN * kBM + quarter * 32 + lane;
         const int m_left = M - m0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = chunk0; c0 < BN; c0 += 64) {
           uint32_t v[32];
           tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
           if (n >= N) continue;
@@ -614,13 +621,13 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         if (lane == 0) mbar_arrive(&tempty[bacc]);
         // the CTA whose stages complete the tile's k-count writes it
         __threadfence();
-        named_bar(1, 128);
+        named_bar(1, kEpiThreads);
         if (et == 0) *s_last = atomicAdd(sk_cnt + sk, k1 - k0) + (k1 - k0) == sch.k_iters;
-        named_bar(1, 128);
+        named_bar(1, kEpiThreads);
         if (*s_last) {
           __threadfence();
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = chunk0; c0 < BN; c0 += 64) {
             if (n >= N) break;
             float dv[32];
 #pragma unroll
@@ -628,7 +635,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
             emit(c0, dv);
           }
         }
-        named_bar(1, 128);                       // s_last is read before the next split tile sets it
+        named_bar(1, kEpiThreads);               // s_last is read before the next split tile sets it
       }
     }
   }
