@@ -41,16 +41,13 @@
 //               the latency-bandwidth product of one SM's share of L2);
 //   warp 1      allocates the 512 TMEM columns and issues tcgen05.mma
 //               (M = 128 weight rows, N = BN tokens, K = 16) from lane 0;
-//               TMEM holds two accumulators (and, from 128 to 224 tokens,
-//               expanded weight stages beside them), or for the 256-token
-//               tile one accumulator and four weight stages;
-//   warps 2..5  expand each packed stage into the fp16 operand (a row per
-//               thread; warp w holds TMEM lanes 32 (w % 4) ..) and arrive at
-//               the stage's named barrier, where the MMA warp syncs: into
-//               TMEM (tcgen05.st) for tiles of 128 to 256 tokens, into a
-//               three-deep shared-memory ring in the canonical
-//               128-byte-swizzled K-major layout for the 32- and 64-token
-//               tiles;
+//               TMEM holds two accumulators and the expanded weight stages
+//               beside them, or for the 256-token tile one accumulator and
+//               four weight stages;
+//   warps 2..5  expand each packed stage into the fp16 operand in TMEM
+//               (tcgen05.st; a row per thread, warp w holds TMEM lanes
+//               32 (w % 4) ..) and arrive at the stage's named barrier,
+//               where the MMA warp syncs;
 //   warps 6..13 epilogue of the previous tile while the MMA fills the other
 //               accumulator (with one accumulator the MMA waits for it, so
 //               two warps share each TMEM lane quarter, taking alternate
@@ -77,7 +74,6 @@ namespace {
 
 constexpr int kBM = 128;                    // weight rows per tile: the MMA's M
 constexpr int kBK = 64;                     // k per stage (one 128-byte fp16 swizzle atom)
-constexpr int kEStages = 3;                 // expanded-weight ring
 constexpr int kExpWarps = 4;                 // expansion: one warp per TMEM lane quarter, a row per thread
 constexpr int kEpiWarps = 8;                 // epilogue: two warps per TMEM lane quarter
 constexpr int kEpiWarp0 = 2 + kExpWarps;     // first epilogue warp
@@ -88,45 +84,40 @@ constexpr int kMaxStages = 10;
 constexpr int kPrefetchStages = 32;         // weight boxes a CTA prefetches into L2 before its dependency wait
 constexpr uint32_t kTmemCols = 512;         // two accumulators of up to 256 columns
 constexpr uint32_t kWpBytes = kBM * kBK / 4;    // 2048
-constexpr uint32_t kWeBytes = kBM * kBK * 2;    // 16384
 // barriers (256 B), then per-token epilogue data for two tiles: scale,
 // reciprocal, token sum (fp32) and per-chunk flags
 constexpr uint32_t kEpiBytes = 3 * kMaxBN * 4 + 64;
 constexpr uint32_t kMiscBytes = 256 + 2 * kEpiBytes;
 constexpr uint32_t kSmemBudget = 232448;    // opt-in shared memory per CTA
-// Where the expanded weights (the MMA's A operand) live. Tiles of 128 to 256
-// tokens keep them in tensor memory, in 32-column slots of one 64-k stage
-// (128 rows x 64 fp16) each: from 128 to 224 tokens at the top of each
-// 256-column half, beside two accumulators (columns [0, BN) and
-// [256, 256 + BN)); at 256 tokens in the upper half, beside one. The expansion
-// warps write them with tcgen05.st, which the MMA may read right after the
-// handoff. Weights written to shared memory instead need a generic-to-async
-// proxy fence before the MMA reads them, and that fence, issued while MMAs
-// are in flight, costs the tensor pipe about 40 % (measured: 225 against 128
-// cycles per 128 x 256 x 16 MMA with the stage handoff alone). The 32- and
-// 64-token tiles keep the shared-memory ring.
-constexpr bool ts_for(int bn) { return bn >= 128 && bn <= 256; }
-// accumulators in TMEM: two (the MMA fills one while the epilogue drains the
-// other), except for the 256-token tile with its weights in TMEM, whose one
-// accumulator takes [0, 256) and leaves [256, 512) to the weight stages
+// The expanded weights (the MMA's A operand) live in tensor memory, in
+// 32-column slots of one 64-k stage (128 rows x 64 fp16) each: for tiles of
+// up to 224 tokens at the top of each 256-column half, beside two
+// accumulators (columns [0, BN) and [256, 256 + BN)); for the 256-token tile
+// in the upper half, beside one accumulator. The expansion warps write them
+// with tcgen05.st, which the MMA may read right after the handoff. Weights
+// written to shared memory instead would need a generic-to-async proxy fence
+// before the MMA reads them, and that fence, issued while MMAs are in flight,
+// costs the tensor pipe about 40 % (measured: 225 against 128 cycles per
+// 128 x 256 x 16 MMA with the stage handoff alone).
+// Accumulators: two (the MMA fills one while the epilogue drains the other),
+// except for the 256-token tile, whose one accumulator takes [0, 256).
 constexpr int acc_bufs(int bn) { return bn == 256 ? 1 : 2; }
+// expanded-weight stages in TMEM
 constexpr int a_stages(int bn) {
   return bn == 256 ? 4 : (2 * ((256 - bn) / 32) < 4 ? 2 * ((256 - bn) / 32) : 4);
 }
-constexpr int e_stages(int bn) { return ts_for(bn) ? a_stages(bn) : kEStages; }
-constexpr uint32_t we_ring_bytes(int bn) { return ts_for(bn) ? 0u : kEStages * kWeBytes; }
 // TMA stage: activation tile [BN][64] fp16, then packed weights [128][16] bytes
 // (a multiple of 1024 bytes, so every swizzled tile stays 1024-aligned).
 constexpr uint32_t stage_bytes(int bn) { return static_cast<uint32_t>(bn) * kBK * 2 + kWpBytes; }
 // As many TMA stages as fit: the ring should hold about one latency's worth
 // of the SM's operand stream whatever the tile width.
 constexpr int stages_for(int bn) {
-  return static_cast<int>((kSmemBudget - 1024 - we_ring_bytes(bn) - kMiscBytes) / stage_bytes(bn)) < kMaxStages
-             ? static_cast<int>((kSmemBudget - 1024 - we_ring_bytes(bn) - kMiscBytes) / stage_bytes(bn))
+  return static_cast<int>((kSmemBudget - 1024 - kMiscBytes) / stage_bytes(bn)) < kMaxStages
+             ? static_cast<int>((kSmemBudget - 1024 - kMiscBytes) / stage_bytes(bn))
              : kMaxStages;
 }
 constexpr uint32_t smem_for(int bn) {
-  return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + we_ring_bytes(bn) + kMiscBytes + 1024;
+  return static_cast<uint32_t>(stages_for(bn)) * stage_bytes(bn) + kMiscBytes + 1024;
 }
 // barriers: full and empty per TMA stage, efree per expanded stage, tfull and
 // tempty per accumulator, then the TMEM base and a flag
@@ -168,19 +159,9 @@ constexpr uint32_t idesc_f16() {
          (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
-template <int BN>
-BL_DEVICE void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc_f16<BN>()), "r"(accumulate)
-      : "memory");
-}
-
-// The same with the A operand (the weights, 128 rows x 16 k of fp16) read
-// from tensor memory: lane = row, two consecutive k per 32-bit column, the
-// lower k in the low half.
+// D (+)= A B^T on the tensor core, A (the weights, 128 rows x 16 k of fp16)
+// from tensor memory (lane = row, two consecutive k per 32-bit column, the
+// lower k in the low half), B (BN tokens x 16 k) from shared memory.
 template <int BN>
 BL_DEVICE void umma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
@@ -202,7 +183,7 @@ BL_DEVICE void named_bar(int id, int count) {
 BL_DEVICE void named_arrive(int id, int count) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// Named barriers 2 .. 2 + e_stages(BN) - 1 (at most 2 .. 5): expanded stage e
+// Named barriers 2 .. 2 + a_stages(BN) - 1 (at most 2 .. 5): expanded stage e
 // is ready (the expansion warps arrive, the MMA warp syncs).
 constexpr int kExpdBar = 2;
 constexpr int kExpdCount = 32 * (kExpWarps + 1);
@@ -309,13 +290,11 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   constexpr int kStages = stages_for(BN);
   constexpr uint32_t kStageBytes = stage_bytes(BN);
   constexpr uint32_t kXBytes = static_cast<uint32_t>(BN) * kBK * 2;
-  constexpr bool kTS = ts_for(BN);               // expanded weights in TMEM
-  constexpr uint32_t kAcc = kTS ? acc_bufs(BN) : 2u;   // TMEM accumulators
-  constexpr int kES = e_stages(BN);              // expanded-weight stages
+  constexpr uint32_t kAcc = acc_bufs(BN);       // TMEM accumulators
+  constexpr int kES = a_stages(BN);              // expanded-weight stages (TMEM)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* we_base = smem + kStages * kStageBytes;               // expanded weights, 1024-aligned (not kTS)
-  uint8_t* misc = we_base + we_ring_bytes(BN);
+  uint8_t* misc = smem + kStages * kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(misc);            // TMA stage landed
   uint64_t* empty = full + kStages;                              // TMA stage consumed by the MMA
   uint64_t* efree = empty + kStages;                             // expanded buffer consumed
@@ -410,17 +389,10 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         tc_fence_after();
         if (lane == 0) {
           const uint64_t bdesc = sw128_desc(smem_u32(smem + s * kStageBytes));   // activations [BN][64]
-          if constexpr (kTS) {
-            const uint32_t a = tmem + a_col<BN>(e);                             // weights, TMEM lanes 0..127
+          const uint32_t a = tmem + a_col<BN>(e);                               // weights, TMEM lanes 0..127
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              umma_f16_ts<BN>(d, a + 8u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
-          } else {
-            const uint64_t adesc = sw128_desc(smem_u32(we_base + e * kWeBytes));  // weights [128][64]
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              umma_f16<BN>(d, adesc + 2u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_f16_ts<BN>(d, a + 8u * kk, bdesc + 2u * kk, (it != k0 || kk != 0) ? 1u : 0u);
           umma_commit(&empty[s]);
           umma_commit(&efree[e]);
         }
@@ -429,7 +401,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       if (lane == 0) umma_commit(&tfull[b]);
       __syncwarp();
     }
-  } else if (warp < kEpiWarp0 && kTS) {
+  } else if (warp < kEpiWarp0) {
     // ---- weight expansion into TMEM: warp w reaches TMEM lanes 32 (w % 4) ..
     // 32 (w % 4) + 31 only, so lane l expands row 32 (w % 4) + l, all 64
     // codes of the stage (32 columns).
@@ -465,35 +437,6 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
         tmem_st32(lane_base + a_col<BN>(e), v);
         tc_fence_before();
-        named_arrive(kExpdBar + static_cast<int>(e), kExpdCount);
-      }
-    }
-  } else if (warp < kEpiWarp0 && !kTS) {
-    // ---- weight expansion: thread r expands row r of each stage (64 codes)
-    const int r = tid - 64;
-    const uint32_t sw = static_cast<uint32_t>(r & 7);
-    uint32_t g = 0;
-    for (int item = 0; item < n_items; ++item) {
-      int tile, k0, k1;
-      sch.item(blockIdx.x, gridDim.x, item, tile, k0, k1);
-      for (int it = k0; it < k1; ++it, ++g) {
-        const uint32_t s = g % kStages, ph = (g / kStages) & 1u;
-        const uint32_t e = g % kES, eph = (g / kES) & 1u;
-        ok = mbar_wait_sleep(&full[s], ph) && ok;
-        if (g >= static_cast<uint32_t>(kES)) ok = mbar_wait_sleep(&efree[e], eph ^ 1u) && ok;
-        const uint4 pw = *reinterpret_cast<const uint4*>(smem + s * kStageBytes + kXBytes + r * 16);
-        uint8_t* row = we_base + e * kWeBytes + r * 128;
-        const uint32_t words[4] = {pw.x, pw.y, pw.z, pw.w};
-#pragma unroll
-        for (uint32_t q = 0; q < 4; ++q) {
-          const uint32_t lo = __byte_perm(words[q], 0u, 0x4140);   // bytes 0, 1 -> 16-bit lanes
-          const uint32_t hi = __byte_perm(words[q], 0u, 0x4342);   // bytes 2, 3
-          const uint4 c0 = make_uint4(lo & 0x00030003u, hi & 0x00030003u, lo & 0x000c000cu, hi & 0x000c000cu);
-          const uint4 c1 = make_uint4(lo & 0x00300030u, hi & 0x00300030u, lo & 0x00c000c0u, hi & 0x00c000c0u);
-          *reinterpret_cast<uint4*>(row + (((2u * q) ^ sw) << 4)) = c0;
-          *reinterpret_cast<uint4*>(row + (((2u * q + 1u) ^ sw) << 4)) = c1;
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         named_arrive(kExpdBar + static_cast<int>(e), kExpdCount);
       }
     }
