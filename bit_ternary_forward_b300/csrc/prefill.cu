@@ -530,38 +530,60 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
         }
       };
       if (tile < sch.dp_tiles) {
-        // a whole tile: straight from TMEM
+        // a whole tile: straight from TMEM. The warp hands the accumulator
+        // back right after its last TMEM load, before that chunk's
+        // arithmetic and stores (with one accumulator the MMA waits for it).
+        bool released = false;
 #pragma unroll 1
         for (int c0 = chunk0; c0 < BN; c0 += 64) {
           uint32_t v[32];
           tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+          if (c0 + 64 >= BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[bacc]);
+            released = true;
+          }
           if (n >= N) continue;
           float dv[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) dv[j] = __uint_as_float(v[j]);
           emit(c0, dv);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[bacc]);
+        if (!released) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[bacc]);
+        }
       } else {
         // part of a split tile: add the partial into the tile's buffer
         // [token][row]; the 32 lanes of a warp add 32 consecutive floats
         const int sk = tile - sch.dp_tiles;
         float* buf = sk_buf + static_cast<size_t>(sk) * BN * kBM + quarter * 32 + lane;
         const int m_left = M - m0;
+        // as for a whole tile, the accumulator goes back after the last TMEM
+        // load, before that chunk's atomic adds
+        bool released = false;
 #pragma unroll 1
         for (int c0 = chunk0; c0 < BN; c0 += 64) {
           uint32_t v[32];
           tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
+          if (c0 + 64 >= BN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[bacc]);
+            released = true;
+          }
           if (n >= N) continue;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (c0 + j < m_left) atomicAdd(buf + static_cast<size_t>(c0 + j) * kBM, __uint_as_float(v[j]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[bacc]);
+        if (!released) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[bacc]);
+        }
         // the CTA whose stages complete the tile's k-count writes it
         __threadfence();
         named_bar(1, kEpiThreads);
