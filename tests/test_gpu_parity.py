@@ -120,6 +120,35 @@ def test_split_tile_contraction(m, n, k):
     compare_full(w, x)
 
 
+# Shapes that select each token-tile width of the tensor-core contraction, whole
+# and split by k-stages, on a 148-SM B300: two accumulators with weight stages
+# beside them (32-224 tokens) and the one-accumulator 256-token tile.
+TILE_CASES = [
+    # (width, split, M, N, K)
+    (32, False, 33, 1024, 512), (32, True, 17, 2560, 2560),
+    (64, False, 65, 1024, 512), (64, True, 33, 2560, 2560),
+    (128, False, 65, 2560, 2560), (128, True, 17, 1024, 512),
+    (160, False, 1000, 2560, 512), (160, True, 129, 1024, 1024),
+    (192, True, 161, 1024, 1024), (224, False, 1500, 2560, 512),
+    (256, False, 193, 2560, 2560), (256, True, 2048, 2560, 2560),
+]
+
+
+@pytest.mark.parametrize("bn,split,m,n,k", TILE_CASES)
+def test_every_tile_width_and_split(bn, split, m, n, k):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan, _ = blt.tc_schedule(m, n, k, sms)
+    if sms == 148:
+        assert (plan.bn, plan.sk_tiles > 0) == (bn, split), plan
+    w = gaussian_weights(n, k, seed=6000 + bn + n)
+    x = gaussian_activations(m, k, seed=6100 + m + k)
+    if m * n * k <= 300_000_000:
+        compare_full(w, x)
+    else:
+        rows = np.sort(np.random.default_rng(bn).choice(m, 40, replace=False))
+        compare_sampled_rows(w, x, np.concatenate([[0, m - 1], rows]))
+
+
 # ------------------------------------------------------------------ degenerate and special values
 def test_zero_token_and_zero_weights():
     w = gaussian_weights(64, 256, seed=5)
