@@ -459,6 +459,7 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
     const int chunk0 = 32 * ((warp - kEpiWarp0) >> 2);
     const float gm = OUT_ACC ? 0.f : __ldg(gamma);
     const bool gamma_fast = OUT_ACC || (gm > 0x1p-72f && gm < 0x1p72f);
+    const float gm24 = __fmul_rn(gm, 16777216.f);   // exact whenever the branch-free form is taken
     uint32_t tcount = 0;
     for (int item = 0; item < n_items; ++item, ++tcount) {
       int tile, k0, k1;
@@ -468,14 +469,15 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const uint32_t bacc = tcount % kAcc;          // accumulator
       float* s_scale = reinterpret_cast<float*>(misc + 256 + b * kEpiBytes);
       float* s_rcp = s_scale + kMaxBN;           // recip_for_div(s): fp32(1/s), or 0 outside 2^-96..2^96
-      float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q as (exact) fp32
+      float* s_rowsum = s_rcp + kMaxBN;          // token sums of x_q times 2^-24 (exact) as fp32
       int* s_fast = reinterpret_cast<int*>(s_rowsum + kMaxBN);   // per 32-token chunk: the branch-free form is exact
       for (int i = et; i < BN; i += kEpiThreads) {
         const int m = m0 + i;
         const float sc = (!OUT_ACC && m < M) ? __ldg(scale + m) : 1.f;
         s_scale[i] = sc;
         s_rcp[i] = recip_for_div(sc);
-        s_rowsum[i] = static_cast<float>(m < M ? __ldg(rowsum + m) : 0);   // |sum| <= 128 K <= 2^23: exact
+        // |sum| <= 128 K <= 2^23: exact, and so is the scaling by 2^-24
+        s_rowsum[i] = __fmul_rn(static_cast<float>(m < M ? __ldg(rowsum + m) : 0), 0x1p-24f);
       }
       for (int c = warp - kEpiWarp0; c < BN / 32; c += kEpiWarps) {
         const int m = m0 + c * 32 + lane;
@@ -497,28 +499,39 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
       const int n = n0 + quarter * 32 + lane;
       float* yrow = OUT_ACC ? nullptr : static_cast<float*>(out) + static_cast<size_t>(m0) * N + n;
       int32_t* arow = OUT_ACC ? static_cast<int32_t*>(out) + static_cast<size_t>(m0) * N + n : nullptr;
-      // y (or acc) of tokens m0 + c0 .. m0 + c0 + 31 of row n from the sums D
+      // y (or acc) of tokens m0 + c0 .. m0 + c0 + 31 of row n from the sums D.
+      // D - rowsum 2^-24 = acc 2^-24 exactly (both multiples of 2^-24, the
+      // difference below 2^23 2^-24); acc 2^-24 times gamma 2^24 is the real
+      // number acc gamma, so t rounds as fp32(acc * gamma).
       auto emit = [&](int c0, const float (&dv)[32]) {
         const bool full_chunk = m0 + c0 + 32 <= M;
         if (full_chunk && s_fast[c0 >> 5]) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
-            const size_t o = static_cast<size_t>(c0 + j) * N;
+          for (int j4 = 0; j4 < 32; j4 += 4) {
+            const float4 rs = *reinterpret_cast<const float4*>(s_rowsum + c0 + j4);   // 16-byte aligned
+            const float rsv[4] = {rs.x, rs.y, rs.z, rs.w};
             if constexpr (OUT_ACC) {
-              arow[o] = static_cast<int>(acc);
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+                arow[static_cast<size_t>(c0 + j4 + jj) * N] =
+                    static_cast<int>(__fmul_rn(__fsub_rn(dv[j4 + jj], rsv[jj]), 16777216.f));
             } else {
-              const float t = __fmul_rn(acc, gm);
-              const float r = s_rcp[c0 + j];
-              const float q = __fmul_rn(t, r);
-              yrow[o] = __fmaf_rn(__fmaf_rn(-q, s_scale[c0 + j], t), r, q);
+              const float4 rc = *reinterpret_cast<const float4*>(s_rcp + c0 + j4);
+              const float4 sc = *reinterpret_cast<const float4*>(s_scale + c0 + j4);
+              const float rcv[4] = {rc.x, rc.y, rc.z, rc.w}, scv[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const float t = __fmul_rn(__fsub_rn(dv[j4 + jj], rsv[jj]), gm24);
+                const float q = __fmul_rn(t, rcv[jj]);
+                yrow[static_cast<size_t>(c0 + j4 + jj) * N] = __fmaf_rn(__fmaf_rn(-q, scv[jj], t), rcv[jj], q);
+              }
             }
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (m0 + c0 + j < M) {
-              const float acc = __fsub_rn(__fmul_rn(dv[j], 16777216.f), s_rowsum[c0 + j]);
+              const float acc = __fmul_rn(__fsub_rn(dv[j], s_rowsum[c0 + j]), 16777216.f);
               const size_t o = static_cast<size_t>(c0 + j) * N;
               if constexpr (OUT_ACC) {
                 arow[o] = static_cast<int>(acc);
