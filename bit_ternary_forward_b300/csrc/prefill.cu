@@ -23,9 +23,10 @@
 //     for K <= 65536, so the fp32 accumulator holds it exactly (as long as
 //     the tensor core adds such multiples of 2^-24 without loss; the GPU
 //     parity tests drive the sum to that bound at K = 65536, on whole and on
-//     split tiles, and compare bit for bit). The epilogue scales by 2^24,
-//     subtracts the token sum of x_q (field = code + 1) and applies
-//     y = fp32(fp32(acc * gamma) / s).
+//     split tiles, and compare bit for bit). The epilogue subtracts the
+//     token sum of x_q times 2^-24 (field = code + 1), which leaves
+//     acc * 2^-24 exactly, and applies y = fp32(fp32(acc * gamma) / s),
+//     taking acc * gamma as (acc * 2^-24) * (gamma * 2^24).
 //
 // Kernel shape: persistent, one CTA per SM, tiles of 128 weight rows x BN
 // tokens, 448 threads. Whole tiles are dealt round-robin; when the last
@@ -443,8 +444,9 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
   } else {
     // ---- epilogue: TMEM lane = weight row, column = token.
     // D = (sum_k field * x_q) * 2^-24 exactly; every value below is an
-    // integer smaller than 2^24 in magnitude, so the fp32 arithmetic is exact
-    // up to the rescale, which rounds as fp32(fp32(acc * gamma) / s).
+    // integer smaller than 2^24 in magnitude times 2^-24 (or an integer), so
+    // the fp32 arithmetic is exact up to the rescale, which rounds as
+    // fp32(fp32(acc * gamma) / s).
     // The reciprocal-and-correction division is exact when t = acc * gamma
     // and the quotient stay in the normal range. With gamma inside
     // 2^-72..2^72, every nonzero |t| lies in gamma..2^24 gamma, inside
