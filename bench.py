@@ -105,7 +105,8 @@ def row_kernels(p):
     else:
         fwd = ["bl_act_quant", "bl_gemv_w2a8"]
     return {"pack_weights": ["bl_absum_partials", "bl_quant_pack"], "forward": fwd, "forward_lut": ["bl_gemv_lut"],
-            "forward_grouped": ["bl_act_quant_grouped", "bl_gemm_grouped"], "pack_grouped": ["bl_pack_grouped"]}
+            "forward_grouped": ["bl_gemv_grouped"] if p.m == 1 else ["bl_act_quant_grouped", "bl_gemm_grouped"],
+            "pack_grouped": ["bl_pack_grouped"]}
 
 
 def workload_units(projs, unit, rows=("forward",)):

@@ -331,28 +331,15 @@ size_t gemm_grouped_smem(int K, int tm) {
          static_cast<size_t>(kGSlices) * kGRows * tm * 8 + 16;
 }
 
+// The contraction of a staged tile (codes s_x [tm][K/16], group code sums
+// s_gs [tm][G]) against weight rows blockIdx.x * 32 .., and y = sum / sc[t]
+// for its tm tokens m0 ...; ends with a CTA barrier before the stores.
 template <int TM>
-__global__ void __launch_bounds__(kGThreads)
-bl_gemm_grouped(const uint8_t* __restrict__ wp, const float* __restrict__ gam, const uint4* __restrict__ xt,
-                const int* __restrict__ gsum, const float* __restrict__ scale, float* __restrict__ y, int M, int N,
-                int K) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  pdl_wait();
-  pdl_launch_dependents();
-  xt = launder(xt);
-  gsum = launder(gsum);
-  scale = launder(scale);
+BL_DEVICE void grouped_tile(const uint4* s_x, const int* s_gs, double* s_part, const uint8_t* __restrict__ wp,
+                            const float* __restrict__ gam, const float* sc, float* __restrict__ y, int m0, int tm,
+                            int N, int K) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = K >> 6, nblk = K >> 4;
-  const int m0 = blockIdx.y * TM;
-  const int tm = min(TM, M - m0);
-  uint4* s_x = reinterpret_cast<uint4*>(smem);                                   // [TM][K/16]
-  int* s_gs = reinterpret_cast<int*>(smem + static_cast<size_t>(TM) * K);        // [TM][G]
-  double* s_part = reinterpret_cast<double*>(
-      (reinterpret_cast<uintptr_t>(s_gs + TM * G) + 7) & ~uintptr_t(7));         // [slices][rows][TM]
-  for (int i = tid; i < tm * nblk; i += kGThreads) s_x[i] = ldg_cg_v4(xt + static_cast<size_t>(m0) * nblk + i);
-  for (int i = tid; i < tm * G; i += kGThreads) s_gs[i] = __ldcg(gsum + static_cast<size_t>(m0) * G + i);
-  __syncthreads();
   const int n = blockIdx.x * kGRows + lane;
   double acc[TM];
 #pragma unroll
@@ -407,9 +394,114 @@ bl_gemm_grouped(const uint8_t* __restrict__ wp, const float* __restrict__ gam, c
     if (nn < N) {
       double v = 0.0;
       for (int sl = 0; sl < kGSlices; ++sl) v += s_part[(sl * kGRows + r) * TM + t];
-      y[static_cast<size_t>(m0 + t) * N + nn] = __double2float_rn(v / static_cast<double>(__ldcg(scale + m0 + t)));
+      y[static_cast<size_t>(m0 + t) * N + nn] = __double2float_rn(v / static_cast<double>(sc[t]));
     }
   }
+}
+
+template <int TM>
+__global__ void __launch_bounds__(kGThreads)
+bl_gemm_grouped(const uint8_t* __restrict__ wp, const float* __restrict__ gam, const uint4* __restrict__ xt,
+                const int* __restrict__ gsum, const float* __restrict__ scale, float* __restrict__ y, int M, int N,
+                int K) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  pdl_wait();
+  pdl_launch_dependents();
+  xt = launder(xt);
+  gsum = launder(gsum);
+  scale = launder(scale);
+  const int tid = threadIdx.x;
+  const int G = K >> 6, nblk = K >> 4;
+  const int m0 = blockIdx.y * TM;
+  const int tm = min(TM, M - m0);
+  uint4* s_x = reinterpret_cast<uint4*>(smem);                                   // [TM][K/16]
+  int* s_gs = reinterpret_cast<int*>(smem + static_cast<size_t>(TM) * K);        // [TM][G]
+  double* s_part = reinterpret_cast<double*>(
+      (reinterpret_cast<uintptr_t>(s_gs + TM * G) + 7) & ~uintptr_t(7));         // [slices][rows][TM]
+  for (int i = tid; i < tm * nblk; i += kGThreads) s_x[i] = ldg_cg_v4(xt + static_cast<size_t>(m0) * nblk + i);
+  for (int i = tid; i < tm * G; i += kGThreads) s_gs[i] = __ldcg(gsum + static_cast<size_t>(m0) * G + i);
+  __syncthreads();
+  grouped_tile<TM>(s_x, s_gs, s_part, wp, gam, scale + m0, y, m0, tm, N, K);
+}
+
+// One token (M = 1) in one kernel: every CTA quantises the token itself
+// (the same absmax, codes and group sums as bl_act_quant_grouped, into shared
+// memory), then contracts its 32 weight rows as bl_gemm_grouped does. The
+// rows' packed words start moving into L2 before the dependency
+// wait (a prefetch cannot change what later loads see). CTA 0 also writes
+// the optional scale and codes.
+template <typename T>
+__global__ void __launch_bounds__(kGThreads)
+bl_gemv_grouped(const T* __restrict__ x, const uint8_t* __restrict__ wp, const float* __restrict__ gam,
+                float* __restrict__ y, int8_t* __restrict__ xq_out, float* __restrict__ scale_out, int N, int K) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float s_red[kGThreads / 32];
+  __shared__ float s_scale;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int G = K >> 6, nblk = K >> 4;
+  if (tid == 0) {
+    // 16-byte aligned, a multiple of 16 bytes: K / 4 is a multiple of 16
+    const int r0 = blockIdx.x * kGRows, rows = min(kGRows, N - r0);
+    prefetch_l2_range(wp + static_cast<size_t>(r0) * (K >> 2), static_cast<uint64_t>(rows) * (K >> 2));
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  x = launder(x);
+  wp = launder(wp);
+  gam = launder(gam);
+  uint4* s_x = reinterpret_cast<uint4*>(smem);                                   // [K/16]
+  int* s_gs = reinterpret_cast<int*>(smem + static_cast<size_t>(K));             // [G]
+  double* s_part = reinterpret_cast<double*>(
+      (reinterpret_cast<uintptr_t>(s_gs + G) + 7) & ~uintptr_t(7));              // [slices][rows]
+  float amax = 0.f;
+  for (int b = tid; b < nblk; b += kGThreads) {
+    float f[16];
+    Block16<T>::load(x, b, f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  }
+  amax = warp_max(amax);
+  if (lane == 0) s_red[tid >> 5] = amax;
+  __syncthreads();
+  const float s = token_scale(warp_max(lane < kGThreads / 32 ? s_red[lane] : 0.f));
+  if (tid == 0) {
+    s_scale = s;
+    if (scale_out && blockIdx.x == 0) scale_out[0] = s;
+  }
+  // blocks 4g .. 4g + 3 (one group) are taken by four consecutive threads
+  const int nb_pad = (nblk + kGThreads - 1) / kGThreads * kGThreads;
+  for (int b = tid; b < nb_pad; b += kGThreads) {
+    int bs = 0;
+    if (b < nblk) {
+      float f[16];
+      Block16<T>::load(x, b, f);
+      uint32_t c[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i] = static_cast<uint32_t>(quant_code(f[i], s)) & 0xffu;
+      uint4 t;
+      t.x = low4(c[0], c[4], c[8], c[12]);
+      t.y = low4(c[1], c[5], c[9], c[13]);
+      t.z = low4(c[2], c[6], c[10], c[14]);
+      t.w = low4(c[3], c[7], c[11], c[15]);
+      s_x[b] = t;
+      bs = dp4a_ss(static_cast<int>(t.w), 0x01010101,
+                   dp4a_ss(static_cast<int>(t.z), 0x01010101,
+                           dp4a_ss(static_cast<int>(t.y), 0x01010101, dp4a_ss(static_cast<int>(t.x), 0x01010101, 0))));
+      if (xq_out && blockIdx.x == 0) {
+        uint4 o;
+        o.x = low4(c[0], c[1], c[2], c[3]);
+        o.y = low4(c[4], c[5], c[6], c[7]);
+        o.z = low4(c[8], c[9], c[10], c[11]);
+        o.w = low4(c[12], c[13], c[14], c[15]);
+        reinterpret_cast<uint4*>(xq_out)[b] = o;
+      }
+    }
+    bs += __shfl_xor_sync(0xffffffffu, bs, 1);
+    bs += __shfl_xor_sync(0xffffffffu, bs, 2);
+    if ((b & 3) == 0 && b < nblk) s_gs[b >> 2] = bs;
+  }
+  __syncthreads();
+  grouped_tile<1>(s_x, s_gs, s_part, wp, gam, &s_scale, y, 0, 1, N, K);
 }
 
 size_t forward_grouped_workspace(int64_t M, int64_t K) {
@@ -420,6 +512,18 @@ size_t forward_grouped_workspace(int64_t M, int64_t K) {
 
 cudaError_t launch_forward_grouped(const void* x, bool bf16, int M, int N, int K, const uint8_t* wp, const float* gam,
                                    float* y, int8_t* xq_out, float* scale_out, void* ws, cudaStream_t s) {
+  if (M == 1) {
+    // one token: one kernel, every CTA quantising the token itself
+    const size_t smem = gemm_grouped_smem(K, 1);
+    const dim3 grid((N + kGRows - 1) / kGRows);
+    auto go1 = [&](auto kern, auto xp) -> cudaError_t {
+      const cudaError_t e1 = ensure_smem(reinterpret_cast<const void*>(kern), smem);
+      if (e1 != cudaSuccess) return e1;
+      return launch_pdl(kern, grid, dim3(kGThreads), smem, s, xp, wp, gam, y, xq_out, scale_out, N, K);
+    };
+    return bf16 ? go1(bl_gemv_grouped<uint16_t>, static_cast<const uint16_t*>(x))
+                : go1(bl_gemv_grouped<float>, static_cast<const float*>(x));
+  }
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint4* xt = reinterpret_cast<uint4*>(base);
   base += (static_cast<size_t>(M) * K + 255) / 256 * 256;
