@@ -810,7 +810,8 @@ def measure_grouped(fs, wl, device, stream, args, world, hbm, dp4a_value):
                   else sum(row_ops(p)["forward_grouped"] for p in wl.projections))
     value = world * units_step * args.steps / (ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
     row = row_entry("forward with per-group (64) scales (each call alone)", per_call, "forward_grouped", hbm)
-    return {"kernels": ["bl_act_quant_grouped", "bl_gemm_grouped"], "value": value, "unit": unit,
+    return {"kernels": sorted({k for p in wl.projections for k in row_kernels(p)["forward_grouped"]}), "value": value,
+            "unit": unit,
             "frac": value / hbm if unit == "GB/s" else None, "ms_per_step": ms / args.steps,
             "alone_us": row["avg_us"], "vs_per_tensor": value / dp4a_value,
             "timing": "the main line's method on the same slots: graph of the step's calls, no event nodes"}, row
