@@ -544,61 +544,75 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
           }
         }
       };
-      if (tile < sch.dp_tiles) {
-        // a whole tile: straight from TMEM. The warp hands the accumulator
-        // back right after its last TMEM load, before that chunk's
-        // arithmetic and stores (with one accumulator the MMA waits for it).
-        bool released = false;
+      // The accumulator goes back to the MMA as early as possible. With two
+      // accumulators the MMA fills the other one meanwhile, so the warp reads
+      // its chunks one at a time and hands the accumulator back right after
+      // its last TMEM load. With one (the 256-token tile) the MMA waits for
+      // it: the warp first moves its first two chunks into the free TMEM
+      // columns above the weight stages ([384, 512), 64 per warp of a lane
+      // quarter) and loads its last two into registers, hands the
+      // accumulator back after those four loads and two stores, and only then
+      // does the arithmetic and the memory traffic of all four.
+      const uint32_t lane_q = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t acc_base = tmem + bacc * 256u + lane_q;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[bacc]);
+      };
+      auto drain = [&](auto&& consume) {
+        if constexpr (kAcc == 1) {
+          const uint32_t spare = tmem + lane_q + 384u + 64u * static_cast<uint32_t>((warp - kEpiWarp0) >> 2);
+          uint32_t v[32], w[32];
+          tmem_ld32(acc_base + static_cast<uint32_t>(chunk0), v);
+          tmem_st32(spare, v);
+          tmem_ld32(acc_base + static_cast<uint32_t>(chunk0 + 64), v);
+          tmem_st32(spare + 32u, v);
+          tmem_ld32(acc_base + static_cast<uint32_t>(chunk0 + 128), v);
+          tmem_ld32(acc_base + static_cast<uint32_t>(chunk0 + 192), w);
+          release();
+          consume(chunk0 + 128, v);
+          consume(chunk0 + 192, w);
+          tmem_ld32(spare, v);
+          consume(chunk0, v);
+          tmem_ld32(spare + 32u, v);
+          consume(chunk0 + 64, v);
+        } else {
+          bool released = false;
 #pragma unroll 1
-        for (int c0 = chunk0; c0 < BN; c0 += 64) {
-          uint32_t v[32];
-          tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
-          if (c0 + 64 >= BN) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[bacc]);
-            released = true;
+          for (int c0 = chunk0; c0 < BN; c0 += 64) {
+            uint32_t v[32];
+            tmem_ld32(acc_base + static_cast<uint32_t>(c0), v);
+            if (c0 + 64 >= BN) {
+              release();
+              released = true;
+            }
+            consume(c0, v);
           }
-          if (n >= N) continue;
+          if (!released) release();
+        }
+      };
+      if (tile < sch.dp_tiles) {
+        // a whole tile: y straight from the accumulator
+        drain([&](int c0, const uint32_t (&v)[32]) {
+          if (n >= N) return;
           float dv[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) dv[j] = __uint_as_float(v[j]);
           emit(c0, dv);
-        }
-        if (!released) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[bacc]);
-        }
+        });
       } else {
         // part of a split tile: add the partial into the tile's buffer
         // [token][row]; the 32 lanes of a warp add 32 consecutive floats
         const int sk = tile - sch.dp_tiles;
         float* buf = sk_buf + static_cast<size_t>(sk) * BN * kBM + quarter * 32 + lane;
         const int m_left = M - m0;
-        // as for a whole tile, the accumulator goes back after the last TMEM
-        // load, before that chunk's atomic adds
-        bool released = false;
-#pragma unroll 1
-        for (int c0 = chunk0; c0 < BN; c0 += 64) {
-          uint32_t v[32];
-          tmem_ld32(tmem + bacc * 256u + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(c0), v);
-          if (c0 + 64 >= BN) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[bacc]);
-            released = true;
-          }
-          if (n >= N) continue;
+        drain([&](int c0, const uint32_t (&v)[32]) {
+          if (n >= N) return;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (c0 + j < m_left) atomicAdd(buf + static_cast<size_t>(c0 + j) * kBM, __uint_as_float(v[j]));
-        }
-        if (!released) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[bacc]);
-        }
+        });
         // the CTA whose stages complete the tile's k-count writes it
         __threadfence();
         named_bar(1, kEpiThreads);
