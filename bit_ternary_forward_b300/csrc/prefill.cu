@@ -50,10 +50,12 @@
 //               32 (w % 4) ..) and arrive at the stage's named barrier,
 //               where the MMA warp syncs;
 //   warps 6..13 epilogue of the previous tile while the MMA fills the other
-//               accumulator (with one accumulator the MMA waits for it, so
-//               two warps share each TMEM lane quarter, taking alternate
-//               32-token chunks): tcgen05.ld 32x32b (TMEM lane = weight
-//               row), stores coalesced along the rows.
+//               accumulator; two warps share each TMEM lane quarter, taking
+//               alternate 32-token chunks: tcgen05.ld 32x32b (TMEM lane =
+//               weight row), stores coalesced along the rows. With one
+//               accumulator each warp first parks half of its chunks in
+//               the TMEM columns the weight stages leave free and hands
+//               the accumulator back before any arithmetic.
 // Every wait on the full / empty stage barriers and on the accumulator
 // barriers is bounded; the named barriers are matched by construction (both
 // sides walk the same schedule). The expansion and epilogue warps sleep
@@ -847,8 +849,9 @@ EncodeTiled encode_fn() {
 // Time of one k-stage of a tile, in units of the 256-token stage with the
 // weights in shared memory, measured on B300 over the 2B and 7B projection
 // shapes at M = 512-2048. The tiles with their weights in TMEM take 0.62
-// (256 tokens, one accumulator, its epilogue not overlapped) to 0.76; the
-// 32- and 64-token tiles keep the earlier estimate.
+// (256 tokens, one accumulator) to 0.76; the 32- and 64-token tiles keep
+// the earlier estimate. (The 256-token tile's figure was measured before its
+// epilogue handed the accumulator back early, which made it 1-4 % faster.)
 constexpr double stage_cost(int bn) {
   return bn == 256 ? 0.62 : bn == 224 ? 0.76 : bn == 192 ? 0.72 : bn == 160 ? 0.70 : bn == 128 ? 0.67 : 0.78;
 }
@@ -872,8 +875,8 @@ TcPlan tc_plan(int M, int N, int K, int sms) {
   double best_cost = -1.0;
   int best_tm = 0;
   for (int bn : cands) {
-    // the 256-token tile's epilogue holds its one accumulator, so it needs
-    // tiles long in k and nearly full in tokens
+    // the 256-token tile has one accumulator, so the MMA still waits for
+    // part of each epilogue: it needs tiles long in k and nearly full in tokens
     if (bn == 256 && (M <= 192 || k_iters < 16)) continue;
     const int tm = (M + bn - 1) / bn;
     const int tiles = tn * tm;
