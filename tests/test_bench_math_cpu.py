@@ -200,3 +200,19 @@ def test_step_sets_build_every_call_kind_on_cpu(monkeypatch):
     assert [n for n in calls if n in ("bitlinear_forward", "bitlinear_forward_lut", "bitlinear_forward_grouped")] == \
         ["bitlinear_forward", "bitlinear_forward_lut", "bitlinear_forward_grouped"]
     assert len(bench.PackSet(FakeBlt, wl.projections, torch.device("cpu"), 2).calls(0)) == len(wl.projections)
+
+
+def test_traffic_records_match_the_kernel_sources():
+    # every DRAM-traffic record the bench reports is keyed to the current
+    # source of its kernel: an edit of the source (or of the shared headers)
+    # must come with a new capture, or a re-keyed record after an edit that
+    # changes no code, else the bench line reports the traffic as null
+    seen = set()
+    with open(bench.TRAFFIC_PATH) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 5 and parts[0] == "traffic":
+                seen.add((parts[1], parts[3]))
+    assert {k for k, _ in seen} == set(bench.KERNEL_SOURCE)
+    for kind, workload in sorted(seen):
+        assert bench.traffic_record(kind, workload) is not None, (kind, workload)
