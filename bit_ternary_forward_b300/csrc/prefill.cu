@@ -719,16 +719,17 @@ template <int XIN> struct Raw16 {
   }
 };
 
-// Codes of one 16-block (fp32 integers q[j] in -128..127 and packed int8
-// words) and its fp16 operand block.
-BL_DEVICE void emit_block(const float (&q)[16], int8_t* xq_row, __half* xp_row, int b, bool write_xq, int& sum) {
+// Codes of one 16-block and its fp16 operand block, from the biased codes
+// e[j] = 1.5 * 2^23 + x_q[16b + j] (exact floats whose low mantissa byte is
+// the code in two's complement).
+BL_DEVICE void emit_block(const float (&e)[16], int8_t* xq_row, __half* xp_row, int b, bool write_xq, int& sum) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t b0 = __float_as_uint(__fadd_rn(q[4 * i], 12582912.f));
-    const uint32_t b1 = __float_as_uint(__fadd_rn(q[4 * i + 1], 12582912.f));
-    const uint32_t b2 = __float_as_uint(__fadd_rn(q[4 * i + 2], 12582912.f));
-    const uint32_t b3 = __float_as_uint(__fadd_rn(q[4 * i + 3], 12582912.f));
+    const uint32_t b0 = __float_as_uint(e[4 * i]);
+    const uint32_t b1 = __float_as_uint(e[4 * i + 1]);
+    const uint32_t b2 = __float_as_uint(e[4 * i + 2]);
+    const uint32_t b3 = __float_as_uint(e[4 * i + 3]);
     w[i] = __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
   }
   if (write_xq) *reinterpret_cast<uint4*>(xq_row + 16 * b) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -736,13 +737,16 @@ BL_DEVICE void emit_block(const float (&q)[16], int8_t* xq_row, __half* xp_row, 
   sum = dp4a_ss(static_cast<int>(w[1]), 0x01010101, sum);
   sum = dp4a_ss(static_cast<int>(w[2]), 0x01010101, sum);
   sum = dp4a_ss(static_cast<int>(w[3]), 0x01010101, sum);
-  // slot 4i + j holds x_q[4j + i] * 4^-i (exact: small integers times powers of two)
+  // slot 4i + j holds x_q[4j + i] * 4^-i: e * 4^-i - 1.5 * 2^23 * 4^-i in one
+  // fused multiply-add, exact (both products are exact and so is their
+  // difference, a small integer times a power of two), then to fp16 (exact)
   uint32_t h[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float sc = i == 0 ? 1.f : (i == 1 ? 0.25f : (i == 2 ? 0.0625f : 0.015625f));
-    const __half2 lo = __floats2half2_rn(__fmul_rn(q[i], sc), __fmul_rn(q[4 + i], sc));
-    const __half2 hi = __floats2half2_rn(__fmul_rn(q[8 + i], sc), __fmul_rn(q[12 + i], sc));
+    const float off = -12582912.f * sc;
+    const __half2 lo = __floats2half2_rn(__fmaf_rn(e[i], sc, off), __fmaf_rn(e[4 + i], sc, off));
+    const __half2 hi = __floats2half2_rn(__fmaf_rn(e[8 + i], sc, off), __fmaf_rn(e[12 + i], sc, off));
     h[2 * i] = *reinterpret_cast<const uint32_t*>(&lo);
     h[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&hi);
   }
@@ -751,10 +755,12 @@ BL_DEVICE void emit_block(const float (&q)[16], int8_t* xq_row, __half* xp_row, 
   dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
-// fp32 integer value of the code of x: clip(rint(fp32(x * s)), -128, 127).
-BL_DEVICE float code_f(float x, float s) {
+// The code of x, clip(rint(fp32(x * s)), -128, 127), biased: 1.5 * 2^23 +
+// the code (the addition rounds the clamped product to the nearest integer,
+// ties to even, and is exact for it).
+BL_DEVICE float code_biased(float x, float s) {
   const float v = fminf(fmaxf(__fmul_rn(x, s), -128.f), 127.f);
-  return __fsub_rn(__fadd_rn(v, 12582912.f), 12582912.f);
+  return __fadd_rn(v, 12582912.f);
 }
 
 }  // namespace
@@ -790,7 +796,7 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
       float q[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        q[j] = static_cast<float>(static_cast<int8_t>((u[j >> 2] >> (8 * (j & 3))) & 0xffu));
+        q[j] = __fadd_rn(static_cast<float>(static_cast<int8_t>((u[j >> 2] >> (8 * (j & 3))) & 0xffu)), 12582912.f);
       emit_block(q, nullptr, xp_row, b, false, sum);
     }
   } else {
@@ -831,7 +837,7 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
         float f[16], q[16];
         cache[c].widen(f);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) q[j] = code_f(f[j], s);
+        for (int j = 0; j < 16; ++j) q[j] = code_biased(f[j], s);
         emit_block(q, xq_row, xp_row, b, xq_out != nullptr, sum);
       }
     }
@@ -841,7 +847,7 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
       float f[16], q[16];
       r.widen(f);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) q[j] = code_f(f[j], s);
+      for (int j = 0; j < 16; ++j) q[j] = code_biased(f[j], s);
       emit_block(q, xq_row, xp_row, b, xq_out != nullptr, sum);
     }
   }
