@@ -702,6 +702,25 @@ template <int XIN> struct Raw16 {
 #pragma unroll
     for (int i = 0; i < kVec; ++i) v[i] = __ldg(p + i);
   }
+  // Folds max|x| of the 16 values into the running maximum: for bf16 as the
+  // unsigned max of the magnitude bits (two 16-bit lanes in `mag`; for
+  // finite values they order like the magnitudes), for fp32 in floats.
+  BL_DEVICE void max_abs(float& amax, uint32_t& mag) const {
+    if constexpr (XIN == kXinBF16) {
+      constexpr uint32_t m = 0x7fff7fffu;
+      const uint32_t a = __vimax3_u16x2(v[0].x & m, v[0].y & m, v[0].z & m);
+      const uint32_t b = __vimax3_u16x2(v[0].w & m, v[1].x & m, v[1].y & m);
+      const uint32_t c = __vimax3_u16x2(v[1].z & m, v[1].w & m, a);
+      mag = __vimax3_u16x2(b, c, mag);
+    } else {
+      float f[16];
+      widen(f);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    }
+  }
+  // The larger magnitude of the two 16-bit lanes as an fp32 value.
+  static BL_DEVICE float mag_to_float(uint32_t mag) { return __uint_as_float(max(mag & 0xffffu, mag >> 16) << 16); }
   BL_DEVICE void widen(float (&f)[16]) const {
 #pragma unroll
     for (int i = 0; i < kVec; ++i) {
@@ -801,26 +820,22 @@ bl_act_perm(const void* __restrict__ x, const float* __restrict__ scale_in, int 
     }
   } else {
     Raw16<XIN> cache[kPermCache];
-    float amax = 0.f;
+    float amax = 0.f;                            // fp32 input: the running max|x|
+    uint32_t mrun = 0u;                          // bf16 input: running max of the magnitude bits
 #pragma unroll
     for (int c = 0; c < kPermCache; ++c) {
       const int b = tid + kPermThreads * c;
       if (b < nblk) {
         cache[c].load(x, row + 16 * b);
-        float f[16];
-        cache[c].widen(f);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        cache[c].max_abs(amax, mrun);
       }
     }
     for (int b = tid + kPermThreads * kPermCache; b < nblk; b += kPermThreads) {
       Raw16<XIN> r;
       r.load(x, row + 16 * b);
-      float f[16];
-      r.widen(f);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+      r.max_abs(amax, mrun);
     }
+    if constexpr (XIN == kXinBF16) amax = Raw16<XIN>::mag_to_float(mrun);
     amax = warp_max(amax);
     if (lane == 0) s_max[warp] = amax;
     __syncthreads();
