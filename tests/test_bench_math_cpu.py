@@ -90,6 +90,13 @@ def test_row_kernels_follow_the_library_dispatch(m, k, want):
     assert bench.row_kernels(proj(m, k, 6912))["forward"] == want
 
 
+@pytest.mark.parametrize("m,want", [(1, ["bl_gemv_grouped"]), (2, ["bl_act_quant_grouped", "bl_gemm_grouped"]),
+                                    (2048, ["bl_act_quant_grouped", "bl_gemm_grouped"])])
+def test_grouped_row_kernels_follow_the_library_dispatch(m, want):
+    # one token: the fused per-group kernel; more: the activation pass, then the contraction
+    assert bench.row_kernels(proj(m, 2560, 6912))["forward_grouped"] == want
+
+
 class _Done:
     def terminate(self):
         pass
