@@ -684,6 +684,8 @@ bl_gemm_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUt
 // t + kPermThreads, ...; the first kPermCache of them (every block up to
 // K = 8192) stay in registers between the absmax reduction (warp shuffles,
 // then one CTA barrier) and the quantisation, so x is read from memory once.
+// For bf16 input the absmax is the unsigned max of the magnitude bits, taken
+// without widening (for finite values the bits order like the magnitudes).
 // Codes are rounded with the 1.5 * 2^23 addition (exact round-to-nearest-even
 // for |v| <= 2^22 after the clamp), which also leaves the code in the low
 // mantissa byte.
